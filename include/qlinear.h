@@ -1,0 +1,207 @@
+/*
+ * qlinear.h - C ABI of the GB300 (sm_103a) quantized decode linear layer.
+ *
+ * Three weight formats of the decode-time weight-quantized linear layer (skinny GEMM,
+ * M = 1..256 tokens), as described by the two source pages:
+ *   [Z100] "Hygon Z100 (gfx906) vLLM adaptation: full record of optimisation and operator
+ *          development (condensed)", chapter 二 (self-written operators) and chapter 三 §2;
+ *   [DSV4] "vLLM 0.27.x port: DeepSeek V4 Flash FP4 on Hygon DCU - full report".
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer (cudaMalloc / PyTorch CUDA memory) owned by
+ *     the caller; the library never allocates, frees or synchronises, and enqueues all work
+ *     on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *   - bf16 tensors are passed as uint16_t bit patterns; fp8 E4M3, packed fp4 E2M1 and
+ *     UE8M0 scales as uint8_t bytes.  All matrices are row-major with an explicit leading
+ *     dimension (elements for bf16/int8/fp8, BYTES for packed fp4).
+ *   - Every argument is validated on the host before any launch.  An invalid call returns
+ *     an error status and launches nothing: no device assert, no silent copy ([Z100] §二.2.4
+ *     "non-unit inner stride is an explicit error"; [Z100] chapter 四 on skinny kernels that
+ *     device-asserted on unsupported sizes).
+ *   - `workspace` is caller-owned device scratch of at least ql_workspace_bytes(...) bytes,
+ *     16-byte aligned.  It must be zeroed once after allocation (ql_workspace_init); the
+ *     kernels leave it reusable.  Calls that share a workspace must not overlap in time.
+ *   - `path_out` (nullable HOST pointer) receives the QL_PATH_* code of the kernel sequence
+ *     that ran: a dispatch marker, so tests can assert which path was taken.
+ *   - Kernels that wait on barriers bound every wait; a wait that runs out sets a flag in
+ *     the workspace status word (read it with ql_read_device_status) and the kernel exits
+ *     cleanly.  Such a call's outputs are undefined.
+ */
+#ifndef QLINEAR_H
+#define QLINEAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QL_API __attribute__((visibility("default")))
+#else
+#define QL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* ql_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  QL_OK = 0,
+  QL_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size            */
+  QL_ERR_UNSUPPORTED = 2, /* valid but not implemented (shape, block size, mode)      */
+  QL_ERR_ALIGNMENT = 3,   /* base pointer / leading dimension not 16-byte aligned     */
+  QL_ERR_WORKSPACE = 4,   /* workspace null or smaller than ql_workspace_bytes()      */
+  QL_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch error)                */
+  QL_ERR_TIMEOUT = 6      /* a bounded device-side wait ran out (ql_read_device_status)*/
+} ql_status;
+
+/* operation ids for ql_workspace_bytes */
+enum { QL_OP_INT8_W8A8 = 1, QL_OP_FP8_BLOCK = 2, QL_OP_MXFP4 = 3, QL_OP_MOE_MXFP4 = 4 };
+
+/* activation modes of the FP8-block and MXFP4 linears */
+enum {
+  QL_ACT_BF16 = 0,      /* bf16 activations used as they are (a_s = 1)                        */
+  QL_ACT_E4M3_1X128 = 1 /* activations quantised per token and per 128-K group to E4M3 with a
+                           UE8M0 power-of-two scale (smallest 2^e with amax <= 448*2^e),
+                           [DSV4] §3.3 quant_config "activation_scheme: dynamic, fmt e4m3,
+                           scale_fmt ue8m0"                                                   */
+};
+
+/* dispatch markers written to *path_out */
+enum {
+  QL_PATH_NONE = 0,
+  QL_PATH_INT8_SKINNY = 1,     /* per-token INT8 quant kernel + tensor-core skinny GEMM      */
+  QL_PATH_FP8_SKINNY = 2,      /* FP8 block skinny GEMM, bf16 activations                   */
+  QL_PATH_FP8_TCGEN05 = 3,     /* 1x128 act quant + tcgen05 block-scaled GEMM (FP8 x FP8)   */
+  QL_PATH_MXFP4_SKINNY = 4,    /* MXFP4 skinny GEMM, bf16 activations                       */
+  QL_PATH_MXFP4_TCGEN05 = 5,   /* 1x128 act quant + tcgen05 block-scaled GEMM (E4M3 x E2M1) */
+  QL_PATH_MOE_MXFP4 = 6        /* routing + dispatch + gate_up/SiLU + down + combine         */
+};
+
+/* device status flags (bitmask) */
+enum { QL_DEV_TIMEOUT = 1u };
+
+QL_API const char* ql_status_string(ql_status s);
+QL_API int ql_version(void);
+
+/*
+ * Bytes of workspace the op needs for these sizes.  Every layout starts with the same
+ * 256 + 4*65536 bytes: the device status word, then the split-K tickets (kept at zero
+ * between calls), so one workspace can serve calls of any op and shape in turn.  M, N, K as in the op; for
+ * QL_OP_MOE_MXFP4: M tokens, N = H (hidden), K = I (expert intermediate), E experts and
+ * topk routed experts per token.  Returns 0 for an unknown op or negative sizes.
+ */
+QL_API size_t ql_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int topk);
+
+/* Zero `bytes` of workspace on `stream` (cudaMemsetAsync).  Call once after allocating. */
+QL_API ql_status ql_workspace_init(void* workspace, size_t bytes, ql_stream_t stream);
+
+/*
+ * Read (and, if clear != 0, reset) the device status word of `workspace`; synchronises
+ * `stream`.  *flags_out receives the QL_DEV_* bits.  Returns QL_ERR_TIMEOUT if the timeout
+ * bit was set, QL_OK otherwise.  Test and debugging aid: the compute calls never read it.
+ */
+QL_API ql_status ql_read_device_status(void* workspace, ql_stream_t stream, int clear, uint32_t* flags_out);
+
+/*
+ * Iteration cap of every bounded device wait (default 1<<20 polls).  A test knob: a small
+ * cap makes waits run out so the timeout path can be exercised without a hung GPU.
+ */
+QL_API void ql_set_wait_limit(uint32_t polls);
+
+/*
+ * INT8 W8A8 linear with dynamic per-token activation quantisation
+ * ([Z100] §二.2 operator table "INT8 W8A8 sdot4" and §二.2.1):
+ *   x_s[m]  = max_k |x[m,k]| / 127                       (fp32 IEEE division)
+ *   x_q[m,k]= clamp(round_half_even(x[m,k] / x_s[m]), -127, 127)   (0 if x_s == 0)
+ *   acc[m,n]= sum_k x_q[m,k] * w[n,k]                    (exact int32)
+ *   y[m,n]  = bf16((acc * x_s[m]) * w_s[n])  then, if bias, y = bf16(y + bias[n])
+ * x: bf16 [M, ldx] (K used); w: int8 [N, ldw], K-contiguous, "not transposed, not
+ * dequantised"; w_scale: fp32 [N] (per channel) or [1] (per tensor, w_scale_len == 1);
+ * bias: nullable bf16 [N]; y: bf16 [M, ldy].
+ * Debug outputs (nullable): acc_out int32 [M, N] (dense, ld N), xq_out int8 [M, K] (ld K),
+ * xs_out fp32 [M].
+ * Requires: M >= 1, N >= 1, K >= 16, K % 16 == 0, ldx >= K, ldw >= K, ldw % 16 == 0,
+ * ldy >= N, 16-byte aligned x and w, |acc| < 2^31 (always true for K <= 133152).
+ */
+QL_API ql_status qlinear_int8_w8a8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                            const int8_t* w, int64_t N, int64_t ldw,
+                            const float* w_scale, int64_t w_scale_len,
+                            const uint16_t* bias, uint16_t* y, int64_t ldy,
+                            int32_t* acc_out, int8_t* xq_out, float* xs_out,
+                            void* workspace, size_t workspace_bytes, ql_stream_t stream,
+                            int* path_out);
+
+/*
+ * FP8 E4M3 weights with block UE8M0 scales ([Z100] §二.2.4 "block-scaled (128x128) FP8
+ * extension"; chapter 三 §2):
+ *   y[m,n] = bf16( sum_kb a_s[m,kb] * 2^(w_scale[n/block_n, kb] - 127)
+ *                        * sum_{k in kb} a[m,k] * e4m3(w[n,k]) )   (+ bias after the cast)
+ * act_mode QL_ACT_BF16: a = x (bf16), a_s = 1.  QL_ACT_E4M3_1X128: a = e4m3 codes and a_s
+ * their UE8M0 scales from the 1x128 quantisation of x (block_k must then be 128).
+ * x: bf16 [M, ldx]; w: E4M3 bytes [N, ldw] (padded rows allowed, e.g. ldw = K + 256);
+ * w_scale: UE8M0 [ceil(N/block_n), ceil(K/block_k)] row-major; y: bf16 [M, ldy].
+ * Debug outputs (nullable, act_mode 1 only): aq_out E4M3 [M, K], as_out UE8M0 [M, ceil(K/128)].
+ * Paths: act_mode 0 -> skinny tensor-core kernel (block_n % 16 == 0, block_k % 64 == 0);
+ *        act_mode 1 -> tcgen05 block-scaled GEMM (block_n == block_k == 128).
+ * Requires K % 16 == 0 (act_mode 1: K % 128 == 0), ldw % 16 == 0, 16-byte aligned x and w.
+ */
+QL_API ql_status qlinear_fp8_block(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                            const uint8_t* w, int64_t N, int64_t ldw,
+                            const uint8_t* w_scale, int block_n, int block_k, int act_mode,
+                            const uint16_t* bias, uint16_t* y, int64_t ldy,
+                            uint8_t* aq_out, uint8_t* as_out,
+                            void* workspace, size_t workspace_bytes, ql_stream_t stream,
+                            int* path_out);
+
+/*
+ * MXFP4 weights: E2M1 codes packed two per byte (element 2i in the LOW nibble of byte i)
+ * with one UE8M0 scale per 32 consecutive K elements of a row ([DSV4] §9.3, MXFP4 expert
+ * weights kept in checkpoint format and dequantised on demand):
+ *   y[m,n] = bf16( sum_k a[m,k] * e2m1(w[n,k]) * 2^(w_scale[n, k/32] - 127) ) (+ bias)
+ * act_mode QL_ACT_BF16: a = x.  QL_ACT_E4M3_1X128: a = e4m3(q[m,k]) * 2^(s[m,k/128]-127).
+ * w: [N, ldw_bytes] (K/2 bytes used); w_scale: [N, lds] (K/32 used).
+ * Paths: act_mode 0 -> skinny tensor-core kernel; act_mode 1 -> tcgen05 GEMM.
+ * Requires K % 32 == 0 (act_mode 1: K % 128 == 0), ldw_bytes % 16 == 0, 16-byte aligned
+ * x and w, lds >= K/32 (act_mode 1: lds % 16 == 0 and 16-byte aligned w_scale).
+ */
+QL_API ql_status qlinear_mxfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                        const uint8_t* w, int64_t N, int64_t ldw_bytes,
+                        const uint8_t* w_scale, int64_t lds, int act_mode,
+                        const uint16_t* bias, uint16_t* y, int64_t ldy,
+                        uint8_t* aq_out, uint8_t* as_out,
+                        void* workspace, size_t workspace_bytes, ql_stream_t stream,
+                        int* path_out);
+
+/*
+ * MXFP4 mixture-of-experts decode layer ([DSV4] §0.1 "M=1 MoE routing Q1", §0.3 grouped
+ * batch MoE, §9.3 MXFP4 emulation experts):
+ *   routing : p = softmax(router_logits[m, :E]); ids = the topk largest logits (ties go to
+ *             the lower expert id), ordered by decreasing logit; weights = p[ids]
+ *             (divided by their sum if renormalize != 0).  Alternatively the caller passes
+ *             topk_ids_in / topk_w_in and router_logits = NULL (exactly one of the two).
+ *   dispatch: (token, slot) pairs grouped by expert, pairs of one expert in pair order.
+ *   gate_up : for pair (m,j) with expert e: g = W13[e][0:I] x_m, u = W13[e][I:2I] x_m,
+ *             h = bf16(silu(g) * u)
+ *   down    : y[m] = bf16( sum_j weight[m,j] * W2[e_(m,j)] h_(m,j) )
+ * x: bf16 [M, H]; router_logits: bf16 [M, E]; topk_ids_in int32 [M, topk];
+ * topk_w_in fp32 [M, topk]; w13: [E, 2I, H/2] packed E2M1, s13: [E, 2I, H/32] UE8M0;
+ * w2: [E, H, I/2], s2: [E, H, I/32]; y: bf16 [M, H] (dense).
+ * Debug outputs (nullable): topk_ids_out int32 [M, topk], topk_w_out fp32 [M, topk],
+ * h_out bf16 [M*topk, I] (row m*topk + j).
+ * Requires 1 <= M <= 16, 1 <= topk <= min(E, 16), E <= 1024, H % 128 == 0, I % 128 == 0,
+ * 16-byte aligned weight pointers.
+ */
+QL_API ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H,
+                            const uint16_t* router_logits, const int32_t* topk_ids_in,
+                            const float* topk_w_in, int E, int topk, int renormalize,
+                            const uint8_t* w13, const uint8_t* s13,
+                            const uint8_t* w2, const uint8_t* s2, int64_t I,
+                            int32_t* topk_ids_out, float* topk_w_out, uint16_t* h_out,
+                            uint16_t* y, void* workspace, size_t workspace_bytes,
+                            ql_stream_t stream, int* path_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QLINEAR_H */

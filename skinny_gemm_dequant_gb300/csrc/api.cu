@@ -1,0 +1,475 @@
+// C ABI of the library (declared in include/qlinear.h): argument validation, workspace
+// layout, and the dispatch of each operation to its kernel sequence.
+#include <cstdio>
+#include <cstring>
+
+#include "gemm_tcgen05.h"
+#include "internal.h"
+
+using namespace ql;
+
+namespace {
+
+uint32_t g_wait_limit = 1u << 20;
+
+inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Workspace layout: [0, 256) status word; [256, 256 + 4*kMaxTickets) split-K tickets, at the
+// same place for every op and shape, so that no call's data region ever overlaps the tickets
+// (the kernels return every ticket to zero); op regions follow, carved in order.
+constexpr size_t kMaxTickets = 65536;
+constexpr size_t kTicketOff = 256;
+constexpr size_t kRegionsOff = kTicketOff + 4 * kMaxTickets;
+
+struct Carver {
+  size_t off = kRegionsOff;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off += al256(bytes);
+    return o;
+  }
+};
+
+template <class T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+ql_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return QL_OK;
+  fprintf(stderr, "qlinear: CUDA error %s\n", cudaGetErrorString(e));
+  return QL_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ skinny plans
+struct SkinnyPlan {
+  int mt;
+  int64_t nb;  // row blocks
+  SplitK sk;
+};
+
+SkinnyPlan skinny_plan(int fmt, int64_t M, int64_t N, int64_t K) {
+  SkinnyPlan p;
+  p.mt = (M <= 8) ? 1 : 2;
+  p.nb = cdiv(N, SK_ROWS);
+  p.sk = skinny_split(fmt, p.mt, p.nb, K);
+  return p;
+}
+
+struct DenseLayout {
+  size_t counters, part, xq, xs, total;
+};
+
+DenseLayout dense_layout(int fmt, int64_t M, int64_t N, int64_t K) {
+  const SkinnyPlan p = skinny_plan(fmt, M, N, K);
+  Carver c;
+  DenseLayout l;
+  l.counters = kTicketOff;
+  l.part = c.take(p.sk.ks > 1 ? (size_t)p.sk.ks * 16 * N * 4 : 0);
+  l.xq = c.take(fmt == FMT_INT8 ? (size_t)M * K : 0);
+  l.xs = c.take(fmt == FMT_INT8 ? (size_t)M * 4 : 0);
+  l.total = c.off;
+  return l;
+}
+
+struct MoeLayout {
+  size_t ids, wts, offsets, pairs, uniq, nuniq, h, o, cnt_gu, part_gu, cnt_dn, part_dn, total;
+  int mt, umax;
+  SplitK gu, dn;
+  int64_t nb_gu, nb_dn;
+};
+
+MoeLayout moe_layout(int64_t M, int64_t H, int64_t I, int E, int topk) {
+  MoeLayout l;
+  const int64_t P = M * topk;
+  l.umax = (int)(P < E ? P : E);
+  l.mt = (M <= 8) ? 1 : 2;
+  l.nb_gu = cdiv(I, 32);
+  l.nb_dn = cdiv(H, SK_ROWS);
+  l.gu = skinny_split(FMT_MXFP4, l.mt, l.nb_gu * l.umax, H);
+  l.dn = skinny_split(FMT_MXFP4, l.mt, l.nb_dn * l.umax, I);
+  Carver c;
+  l.ids = c.take(P * 4);
+  l.wts = c.take(P * 4);
+  l.offsets = c.take((E + 1) * 4);
+  l.pairs = c.take(P * 4);
+  l.uniq = c.take((size_t)E * 4);
+  l.nuniq = c.take(4);
+  l.h = c.take((size_t)P * I * 2);
+  l.o = c.take((size_t)P * H * 4);
+  l.cnt_gu = kTicketOff;  // gate_up and down run one after the other and share the tickets
+  l.part_gu = c.take(l.gu.ks > 1 ? (size_t)l.umax * l.gu.ks * 16 * (2 * I) * 4 : 0);
+  l.cnt_dn = kTicketOff;
+  l.part_dn = c.take(l.dn.ks > 1 ? (size_t)l.umax * l.dn.ks * 16 * H * 4 : 0);
+  l.total = c.off;
+  return l;
+}
+
+// workspace for the tcgen05 path (activation codes and scales) plus the skinny fallbacks
+size_t act_quant_ws(int64_t M, int64_t K) {
+  Carver c;
+  c.take(tc::act_q_bytes(M, K));
+  c.take(tc::act_s_bytes(M, K));
+  return c.off;
+}
+
+bool tc_path(int act_mode) { return act_mode == QL_ACT_E4M3_1X128; }
+
+}  // namespace
+
+uint32_t ql::wait_limit() { return g_wait_limit; }
+
+extern "C" {
+
+const char* ql_status_string(ql_status s) {
+  switch (s) {
+    case QL_OK: return "ok";
+    case QL_ERR_INVALID_ARG: return "invalid argument";
+    case QL_ERR_UNSUPPORTED: return "unsupported shape or mode";
+    case QL_ERR_ALIGNMENT: return "misaligned pointer or leading dimension";
+    case QL_ERR_WORKSPACE: return "workspace missing or too small";
+    case QL_ERR_CUDA: return "CUDA error";
+    case QL_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int ql_version(void) { return 1; }
+
+void ql_set_wait_limit(uint32_t polls) { g_wait_limit = polls; }
+
+size_t ql_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int topk) {
+  if (M < 0 || N < 0 || K < 0) return 0;
+  const int64_t Mc = M < 16 ? M : 16;  // skinny kernels run 16 tokens at a time
+  switch (op) {
+    case QL_OP_INT8_W8A8: {
+      DenseLayout l = dense_layout(FMT_INT8, Mc, N, K);
+      // the quantised activations of all M tokens live in the workspace
+      Carver c;
+      c.off = l.total;
+      c.take((size_t)M * K);
+      c.take((size_t)M * 4);
+      return c.off;
+    }
+    case QL_OP_FP8_BLOCK: {
+      const size_t a = dense_layout(FMT_FP8, Mc, N, K).total;
+      const size_t b = act_quant_ws(M, K);
+      return a > b ? a : b;
+    }
+    case QL_OP_MXFP4: {
+      const size_t a = dense_layout(FMT_MXFP4, Mc, N, K).total;
+      const size_t b = act_quant_ws(M, K);
+      return a > b ? a : b;
+    }
+    case QL_OP_MOE_MXFP4:
+      if (E <= 0 || topk <= 0) return 0;
+      return moe_layout(M, N, K, E, topk).total;
+  }
+  return 0;
+}
+
+ql_status ql_workspace_init(void* workspace, size_t bytes, ql_stream_t stream) {
+  if (!workspace || bytes < 256) return QL_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream));
+}
+
+ql_status ql_read_device_status(void* workspace, ql_stream_t stream, int clear, uint32_t* flags_out) {
+  if (!workspace) return QL_ERR_WORKSPACE;
+  uint32_t flags = 0;
+  cudaError_t e = cudaMemcpyAsync(&flags, workspace, 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(workspace, 0, 4, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (flags_out) *flags_out = flags;
+  return (flags & QL_DEV_TIMEOUT) ? QL_ERR_TIMEOUT : QL_OK;
+}
+
+// ------------------------------------------------------------------ INT8 W8A8
+ql_status qlinear_int8_w8a8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const int8_t* w, int64_t N,
+                            int64_t ldw, const float* w_scale, int64_t w_scale_len, const uint16_t* bias,
+                            uint16_t* y, int64_t ldy, int32_t* acc_out, int8_t* xq_out, float* xs_out,
+                            void* workspace, size_t workspace_bytes, ql_stream_t stream, int* path_out) {
+  if (path_out) *path_out = QL_PATH_NONE;
+  if (!x || !w || !w_scale || !y) return QL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldx < K || ldw < K || ldy < N) return QL_ERR_INVALID_ARG;
+  if (w_scale_len != 1 && w_scale_len != N) return QL_ERR_INVALID_ARG;
+  if (M > 65535 || N > (1 << 30) || K > 133152) return QL_ERR_UNSUPPORTED;  // |acc| < 2^31
+  if (K % 16 != 0) return QL_ERR_UNSUPPORTED;
+  if (cdiv(N, SK_ROWS) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
+  if (!al16(x) || !al16(w) || ldx % 8 != 0 || ldw % 16 != 0) return QL_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < ql_workspace_bytes(QL_OP_INT8_W8A8, M, N, K, 0, 0)) return QL_ERR_WORKSPACE;
+  if (!al16(workspace)) return QL_ERR_ALIGNMENT;
+  cudaStream_t st = (cudaStream_t)stream;
+
+  const int64_t Mc0 = M < 16 ? M : 16;
+  const DenseLayout lay = dense_layout(FMT_INT8, Mc0, N, K);
+  Carver c;
+  c.off = lay.total;
+  const size_t off_xq = c.take((size_t)M * K), off_xs = c.take((size_t)M * 4);
+  int8_t* xq = at<int8_t>(workspace, off_xq);
+  float* xs = at<float>(workspace, off_xs);
+  cudaError_t e = launch_quant_int8(x, (int)M, (int)K, ldx, xq, xs, xq_out, xs_out, st);
+  if (e != cudaSuccess) return cuda_status(e);
+
+  for (int64_t m0 = 0; m0 < M; m0 += 16) {
+    const int64_t Mc = (M - m0) < 16 ? (M - m0) : 16;
+    const SkinnyPlan p = skinny_plan(FMT_INT8, Mc, N, K);
+    const DenseLayout l = dense_layout(FMT_INT8, Mc, N, K);
+    SkinnyArgs a = {};
+    a.w = reinterpret_cast<const uint8_t*>(w);
+    a.ldw = ldw;
+    a.w_scale = w_scale;
+    a.w_scale_len = (int)w_scale_len;
+    a.x = xq + m0 * K;
+    a.ldx = K;
+    a.x_s = xs + m0;
+    a.M = (int)Mc;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.y = y + m0 * ldy;
+    a.ldy = ldy;
+    a.bias = bias;
+    a.acc_out = acc_out ? acc_out + m0 * N : nullptr;
+    a.ks = p.sk.ks;
+    a.kc = p.sk.kc;
+    a.part = at<void>(workspace, l.part);
+    a.counters = at<unsigned>(workspace, l.counters);
+    a.pdl = 1;
+    e = launch_skinny(FMT_INT8, p.mt, EPI_INT8, a, dim3((unsigned)p.nb, (unsigned)p.sk.ks, 1), st, true);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  if (path_out) *path_out = QL_PATH_INT8_SKINNY;
+  return QL_OK;
+}
+
+// ------------------------------------------------------------------ shared skinny launcher (FP8 / MXFP4, bf16 act)
+static ql_status run_skinny_bf16(int fmt, const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const uint8_t* w,
+                                 int64_t N, int64_t ldw, const uint8_t* wsb, int64_t lds, int block_n, int block_k,
+                                 const uint16_t* bias, uint16_t* y, int64_t ldy, void* workspace, cudaStream_t st) {
+  for (int64_t m0 = 0; m0 < M; m0 += 16) {
+    const int64_t Mc = (M - m0) < 16 ? (M - m0) : 16;
+    const SkinnyPlan p = skinny_plan(fmt, Mc, N, K);
+    const DenseLayout l = dense_layout(fmt, Mc, N, K);
+    SkinnyArgs a = {};
+    a.w = w;
+    a.ldw = ldw;
+    a.wsb = wsb;
+    a.lds = lds;
+    a.block_n = block_n;
+    a.block_k = block_k;
+    a.x = x + m0 * ldx;
+    a.ldx = ldx;
+    a.M = (int)Mc;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.y = y + m0 * ldy;
+    a.ldy = ldy;
+    a.bias = bias;
+    a.ks = p.sk.ks;
+    a.kc = p.sk.kc;
+    a.part = at<void>(workspace, l.part);
+    a.counters = at<unsigned>(workspace, l.counters);
+    a.pdl = 0;
+    cudaError_t e = launch_skinny(fmt, p.mt, EPI_LINEAR, a, dim3((unsigned)p.nb, (unsigned)p.sk.ks, 1), st, false);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return QL_OK;
+}
+
+// ------------------------------------------------------------------ FP8 block
+ql_status qlinear_fp8_block(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const uint8_t* w, int64_t N,
+                            int64_t ldw, const uint8_t* w_scale, int block_n, int block_k, int act_mode,
+                            const uint16_t* bias, uint16_t* y, int64_t ldy, uint8_t* aq_out, uint8_t* as_out,
+                            void* workspace, size_t workspace_bytes, ql_stream_t stream, int* path_out) {
+  if (path_out) *path_out = QL_PATH_NONE;
+  if (!x || !w || !w_scale || !y) return QL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldx < K || ldw < K || ldy < N || block_n < 1 || block_k < 1)
+    return QL_ERR_INVALID_ARG;
+  if (act_mode != QL_ACT_BF16 && act_mode != QL_ACT_E4M3_1X128) return QL_ERR_INVALID_ARG;
+  if (M > 65535 || N > (1 << 30) || K > (1 << 30)) return QL_ERR_UNSUPPORTED;
+  if (K % 16 != 0 || cdiv(N, SK_ROWS) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
+  if (!al16(x) || !al16(w) || ldx % 8 != 0 || ldw % 16 != 0) return QL_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < ql_workspace_bytes(QL_OP_FP8_BLOCK, M, N, K, 0, 0)) return QL_ERR_WORKSPACE;
+  if (!al16(workspace)) return QL_ERR_ALIGNMENT;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!tc_path(act_mode)) {
+    if (block_n % 16 != 0 || block_k % 64 != 0) return QL_ERR_UNSUPPORTED;
+    const ql_status s = run_skinny_bf16(FMT_FP8, x, M, K, ldx, w, N, ldw, w_scale, cdiv(K, block_k), block_n,
+                                        block_k, bias, y, ldy, workspace, st);
+    if (s == QL_OK && path_out) *path_out = QL_PATH_FP8_SKINNY;
+    return s;
+  }
+  if (block_n != 128 || block_k != 128 || K % 128 != 0) return QL_ERR_UNSUPPORTED;
+  Carver c;
+  const size_t oq = c.take(tc::act_q_bytes(M, K)), os = c.take(tc::act_s_bytes(M, K));
+  tc::GemmArgs g = {};
+  g.M = (int)M;
+  g.N = (int)N;
+  g.K = (int)K;
+  g.w = w;
+  g.ldw = ldw;
+  g.ws = w_scale;
+  g.lds = cdiv(K, 128);
+  g.fp4 = 0;
+  g.aq = at<uint8_t>(workspace, oq);
+  g.as = at<uint8_t>(workspace, os);
+  g.y = y;
+  g.ldy = ldy;
+  g.bias = bias;
+  g.status = at<uint32_t>(workspace, 0);
+  g.wait_limit = g_wait_limit;
+  cudaError_t e = tc::quantize_activations(x, M, K, ldx, g, aq_out, as_out, st);
+  if (e == cudaSuccess) e = tc::launch_gemm(g, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (path_out) *path_out = QL_PATH_FP8_TCGEN05;
+  return QL_OK;
+}
+
+// ------------------------------------------------------------------ MXFP4 dense
+ql_status qlinear_mxfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const uint8_t* w, int64_t N,
+                        int64_t ldw_bytes, const uint8_t* w_scale, int64_t lds, int act_mode, const uint16_t* bias,
+                        uint16_t* y, int64_t ldy, uint8_t* aq_out, uint8_t* as_out, void* workspace,
+                        size_t workspace_bytes, ql_stream_t stream, int* path_out) {
+  if (path_out) *path_out = QL_PATH_NONE;
+  if (!x || !w || !w_scale || !y) return QL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldx < K || ldw_bytes * 2 < K || lds * 32 < K || ldy < N) return QL_ERR_INVALID_ARG;
+  if (act_mode != QL_ACT_BF16 && act_mode != QL_ACT_E4M3_1X128) return QL_ERR_INVALID_ARG;
+  if (M > 65535 || N > (1 << 30) || K > (1 << 30)) return QL_ERR_UNSUPPORTED;
+  if (K % 32 != 0 || cdiv(N, SK_ROWS) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
+  if (!al16(x) || !al16(w) || ldx % 8 != 0 || ldw_bytes % 16 != 0) return QL_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < ql_workspace_bytes(QL_OP_MXFP4, M, N, K, 0, 0)) return QL_ERR_WORKSPACE;
+  if (!al16(workspace)) return QL_ERR_ALIGNMENT;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (!tc_path(act_mode)) {
+    if (lds % 4 != 0 || (reinterpret_cast<uintptr_t>(w_scale) & 3) != 0) return QL_ERR_ALIGNMENT;
+    const ql_status s = run_skinny_bf16(FMT_MXFP4, x, M, K, ldx, w, N, ldw_bytes, w_scale, lds, 0, 0, bias, y, ldy,
+                                        workspace, st);
+    if (s == QL_OK && path_out) *path_out = QL_PATH_MXFP4_SKINNY;
+    return s;
+  }
+  if (K % 128 != 0) return QL_ERR_UNSUPPORTED;
+  if (lds % 16 != 0 || !al16(w_scale)) return QL_ERR_ALIGNMENT;
+  Carver c;
+  const size_t oq = c.take(tc::act_q_bytes(M, K)), os = c.take(tc::act_s_bytes(M, K));
+  tc::GemmArgs g = {};
+  g.M = (int)M;
+  g.N = (int)N;
+  g.K = (int)K;
+  g.w = w;
+  g.ldw = ldw_bytes;
+  g.ws = w_scale;
+  g.lds = lds;
+  g.fp4 = 1;
+  g.aq = at<uint8_t>(workspace, oq);
+  g.as = at<uint8_t>(workspace, os);
+  g.y = y;
+  g.ldy = ldy;
+  g.bias = bias;
+  g.status = at<uint32_t>(workspace, 0);
+  g.wait_limit = g_wait_limit;
+  cudaError_t e = tc::quantize_activations(x, M, K, ldx, g, aq_out, as_out, st);
+  if (e == cudaSuccess) e = tc::launch_gemm(g, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (path_out) *path_out = QL_PATH_MXFP4_TCGEN05;
+  return QL_OK;
+}
+
+// ------------------------------------------------------------------ MoE
+ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint16_t* router_logits,
+                            const int32_t* topk_ids_in, const float* topk_w_in, int E, int topk, int renormalize,
+                            const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, int64_t I,
+                            int32_t* topk_ids_out, float* topk_w_out, uint16_t* h_out, uint16_t* y,
+                            void* workspace, size_t workspace_bytes, ql_stream_t stream, int* path_out) {
+  if (path_out) *path_out = QL_PATH_NONE;
+  if (!x || !w13 || !s13 || !w2 || !s2 || !y) return QL_ERR_INVALID_ARG;
+  if ((router_logits == nullptr) == (topk_ids_in == nullptr)) return QL_ERR_INVALID_ARG;
+  if (topk_ids_in && !topk_w_in) return QL_ERR_INVALID_ARG;
+  if (M < 1 || H < 1 || I < 1 || E < 1 || topk < 1) return QL_ERR_INVALID_ARG;
+  if (M > 16 || topk > 16 || topk > E || E > 1024) return QL_ERR_UNSUPPORTED;
+  if (H % 128 != 0 || I % 128 != 0 || H > (1 << 20) || I > (1 << 20)) return QL_ERR_UNSUPPORTED;
+  if (!al16(x) || !al16(w13) || !al16(w2) || (reinterpret_cast<uintptr_t>(s13) & 3) ||
+      (reinterpret_cast<uintptr_t>(s2) & 3))
+    return QL_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < ql_workspace_bytes(QL_OP_MOE_MXFP4, M, H, I, E, topk)) return QL_ERR_WORKSPACE;
+  if (!al16(workspace)) return QL_ERR_ALIGNMENT;
+  cudaStream_t st = (cudaStream_t)stream;
+  const MoeLayout l = moe_layout(M, H, I, E, topk);
+  if ((int64_t)l.umax * (l.nb_gu > l.nb_dn ? l.nb_gu : l.nb_dn) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
+
+  MoeRouteArgs r = {};
+  r.logits = router_logits;
+  r.ids_in = topk_ids_in;
+  r.w_in = topk_w_in;
+  r.M = (int)M;
+  r.E = E;
+  r.topk = topk;
+  r.renorm = renormalize;
+  r.ids = at<int32_t>(workspace, l.ids);
+  r.wts = at<float>(workspace, l.wts);
+  r.offsets = at<int32_t>(workspace, l.offsets);
+  r.pairs = at<int32_t>(workspace, l.pairs);
+  r.uniq = at<int32_t>(workspace, l.uniq);
+  r.nuniq = at<int32_t>(workspace, l.nuniq);
+  r.ids_dbg = topk_ids_out;
+  r.w_dbg = topk_w_out;
+  r.status = at<uint32_t>(workspace, 0);
+  cudaError_t e = launch_moe_route(r, st);
+  if (e != cudaSuccess) return cuda_status(e);
+
+  SkinnyArgs a = {};
+  a.offsets = r.offsets;
+  a.pairs = r.pairs;
+  a.uniq = r.uniq;
+  a.nuniq = r.nuniq;
+  a.topk = topk;
+  a.I = (int)I;
+  a.h = at<uint16_t>(workspace, l.h);
+  a.h_dbg = h_out;
+  a.o = at<float>(workspace, l.o);
+  a.pdl = 1;
+  // gate_up: rows 2I of W13[e], K = H, activations x[m]
+  a.w = w13;
+  a.ldw = H / 2;
+  a.w_estride = 2 * I * (H / 2);
+  a.wsb = s13;
+  a.lds = H / 32;
+  a.s_estride = 2 * I * (H / 32);
+  a.x = x;
+  a.ldx = H;
+  a.M = (int)M;
+  a.N = (int)(2 * I);
+  a.K = (int)H;
+  a.ks = l.gu.ks;
+  a.kc = l.gu.kc;
+  a.part = at<void>(workspace, l.part_gu);
+  a.counters = at<unsigned>(workspace, l.cnt_gu);
+  e = launch_skinny(FMT_MXFP4, l.mt, EPI_GATEUP, a, dim3((unsigned)l.nb_gu, (unsigned)l.gu.ks, (unsigned)l.umax), st,
+                    true);
+  if (e != cudaSuccess) return cuda_status(e);
+  // down: rows H of W2[e], K = I, activations h[pair]
+  a.w = w2;
+  a.ldw = I / 2;
+  a.w_estride = H * (I / 2);
+  a.wsb = s2;
+  a.lds = I / 32;
+  a.s_estride = H * (I / 32);
+  a.x = at<uint16_t>(workspace, l.h);
+  a.ldx = I;
+  a.N = (int)H;
+  a.K = (int)I;
+  a.ks = l.dn.ks;
+  a.kc = l.dn.kc;
+  a.part = at<void>(workspace, l.part_dn);
+  a.counters = at<unsigned>(workspace, l.cnt_dn);
+  e = launch_skinny(FMT_MXFP4, l.mt, EPI_DOWN, a, dim3((unsigned)l.nb_dn, (unsigned)l.dn.ks, (unsigned)l.umax), st,
+                    true);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = launch_moe_combine(at<float>(workspace, l.o), r.ids, r.wts, (int)M, topk, (int)H, y, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (path_out) *path_out = QL_PATH_MOE_MXFP4;
+  return QL_OK;
+}
+
+}  // extern "C"

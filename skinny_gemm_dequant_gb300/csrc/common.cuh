@@ -1,0 +1,118 @@
+// Shared device helpers of the sm_103a quantized linear kernels: raw loads, format
+// conversions, the legacy-path tensor-core fragment MMA, PDL controls, bounded waits.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qlinear.h"
+
+namespace ql {
+
+// ------------------------------------------------------------------ status word
+// workspace[0..255] : [0] status flags, [1] reserved, [16..63] split-K tile counters
+// (tile counters grow beyond 64 entries into the op-specific region when needed).
+struct DevStatus {
+  uint32_t flags;
+};
+
+__device__ __forceinline__ void raise_flag(uint32_t* status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ------------------------------------------------------------------ loads
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  // weights are read exactly once: do not allocate them in L1
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// ------------------------------------------------------------------ bf16 / fp16 helpers
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// fp32 -> bf16, round to nearest even (NaN kept quiet)
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// two E4M3 bytes (low byte -> low lane) to an exact f16x2
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
+  return r;
+}
+
+// one byte holding two E2M1 codes (low nibble -> low lane) to an exact f16x2
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "r"(byte_in_low_bits));
+  return r;
+}
+
+// four signed int8 (one word) to two exact f16x2: lanes (b0,b1) and (b2,b3).
+// 0x6400 | u is the f16 value 1024 + u for u in [0,255]; with u = b + 128 (xor 0x80)
+// subtracting 1152 returns b exactly.
+__device__ __forceinline__ void s8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x7170;" : "=r"(a) : "r"(u), "r"(0x64646464u));   // bytes 0,1
+  asm("prmt.b32 %0, %1, %2, 0x7372;" : "=r"(b) : "r"(u), "r"(0x64646464u));   // bytes 2,3
+  const uint32_t bias = 0x64806480u;                                            // 1152, 1152
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
+}
+
+// UE8M0 byte -> fp32 2^(b-127); b = 0 gives the fp32 subnormal 2^-127, b = 255 NaN
+__device__ __forceinline__ float ue8m0_to_f32(uint32_t b) {
+  b &= 0xFFu;
+  if (b == 0) return __uint_as_float(0x00400000u);
+  if (b == 255) return __uint_as_float(0x7FC00000u);
+  return __uint_as_float(b << 23);
+}
+
+// ------------------------------------------------------------------ warp MMA (f16 -> f32)
+// D[16x8] += A[16x16] * B[16x8]; A row-major fragments a0..a3, B "col" fragments b0,b1.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------------------ programmatic dependent launch
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+
+}  // namespace ql

@@ -1,0 +1,343 @@
+// Block-scaled GEMM on the 5th-generation tensor cores (tcgen05) for batched decode/prefill
+// (M >= 17 tokens) with 1x128 E4M3 activations, FP8-E4M3 or MXFP4 (E2M1) weights.
+//
+// Formula ([Z100] §二.2.4 / chapter 三 §2, block-scaled FP8):
+//   y[m,n] = sum_kb a_s[m,kb] * w_s[n/128,kb] * sum_{k in kb} a[m,k] w[n,k]
+// and for MXFP4 weights ([DSV4] §9.3) the weight scale is per row and per 32 K.  Every scale is
+// a power of two (UE8M0), so applying them per 32-K MMA step inside the tensor core
+// (kind::mxf8f6f4 .block_scale, one scale byte per row and per 32 K) gives exactly the formula.
+//
+// Mapping (swap-AB): the MMA's A operand is a 128-row weight tile, its N dimension is the token
+// tile (16..256), so D[128 x tokens] lives in tensor memory, 1 fp32 column per token.
+// Roles inside a CTA of 8 warps:
+//   warp 0     : TMA producer (weights and activation codes, 128 K per stage, 128B swizzle);
+//   warp 1     : tensor-memory allocation and the single MMA-issuing thread;
+//   warps 4..7 : write the per-stage UE8M0 scale vectors into tensor memory (tcgen05.st),
+//                then the epilogue (tcgen05.ld -> bf16 -> global).
+// Every mbarrier wait is bounded; a wait that runs out raises QL_DEV_TIMEOUT in the status word,
+// the other roles stop, copies and MMAs still in flight are waited for, and tensor memory is
+// freed before the CTA exits.
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "gemm_tcgen05.h"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace ql {
+namespace tc {
+
+constexpr int kThreads = 256;
+constexpr int kBlockN = 128;  // weight rows per CTA (MMA M)
+constexpr int kBlockK = 128;  // K elements per stage
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol0 = 256;  // scale vectors live after the (<= 256-column) accumulator
+constexpr uint32_t kDrainLimit = 1u << 22;
+
+struct TcParams {
+  int M, N, K;
+  int tt, nsub, sub_n, stages;
+  int fp4;
+  const uint8_t* ws;
+  int64_t lds;
+  const uint8_t* as;
+  int64_t las;
+  uint16_t* y;
+  int64_t ldy;
+  const uint16_t* bias;
+  uint32_t* status;
+  uint32_t wait_limit;
+  int sf_layout;  // 0: row r at (lane r % 32 of every quadrant, column r / 32); 1: (lane r, column 0)
+};
+
+__device__ __forceinline__ uint32_t rep4(uint32_t b) { return (b & 0xFFu) * 0x01010101u; }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages;
+  const uint32_t a_bytes = kBlockN * kBlockK;          // 16 KB of A per stage (fp4 unpacked to bytes)
+  const uint32_t b_bytes = (uint32_t)p.tt * kBlockK;   // tokens x 128 B
+  // transaction bytes of the A load: packed fp4 counts the bytes read (8 KB), not the padded
+  // shared-memory image it expands to
+  const uint32_t a_tx = p.fp4 ? a_bytes / 2 : a_bytes;
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + (size_t)S * a_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)S * b_bytes);
+  uint64_t* tma_full = bars;
+  uint64_t* sf_full = bars + S;
+  uint64_t* empty = bars + 2 * S;
+  uint64_t* acc_full = bars + 3 * S;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBlockN;
+  const int t0 = blockIdx.y * p.tt;
+  const int nk = p.K / kBlockK;
+  const uint32_t lim = p.wait_limit;
+  volatile int* abort = &s_abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&tma_full[s], 1);
+      mbar_init(&sf_full[s], 4);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    fence_mbar_init();
+    s_abort = 0;
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  auto fail = [&]() {
+    atomicOr(p.status, (uint32_t)QL_DEV_TIMEOUT);
+    *abort = 1;
+  };
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer
+    const int pre = nk < S ? nk : S;
+    for (int kt = 0; kt < pre; ++kt) {  // weights do not depend on the previous kernel
+      mbar_arrive_expect_tx(&tma_full[kt], a_tx + b_bytes);
+      tma_load_2d(sA + (size_t)kt * a_bytes, &tmA, kt * kBlockK, n0, &tma_full[kt]);
+    }
+    pdl_wait();  // activation codes come from the quantisation kernel
+    for (int kt = 0; kt < pre; ++kt) tma_load_2d(sB + (size_t)kt * b_bytes, &tmB, kt * kBlockK, t0, &tma_full[kt]);
+    int issued = pre;
+    for (int kt = pre; kt < nk; ++kt) {
+      const int s = kt % S;
+      const uint32_t it = kt / S;
+      if (!mbar_wait(&empty[s], (it - 1) & 1, lim, abort)) {
+        fail();
+        break;
+      }
+      mbar_arrive_expect_tx(&tma_full[s], a_tx + b_bytes);
+      tma_load_2d(sA + (size_t)s * a_bytes, &tmA, kt * kBlockK, n0, &tma_full[s]);
+      tma_load_2d(sB + (size_t)s * b_bytes, &tmB, kt * kBlockK, t0, &tma_full[s]);
+      issued = kt + 1;
+    }
+    if (*abort) {
+      // no copy may land after the CTA exits: wait for the last load of every stage
+      for (int kt = issued - S < 0 ? 0 : issued - S; kt < issued; ++kt)
+        mbar_wait(&tma_full[kt % S], (uint32_t)(kt / S) & 1, kDrainLimit, nullptr);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t a_fmt = p.fp4 ? 5u : 0u;  // E2M1 or E4M3
+    for (int kt = 0; kt < nk; ++kt) {
+      const int s = kt % S;
+      const uint32_t par = (uint32_t)(kt / S) & 1;
+      if (!mbar_wait(&tma_full[s], par, lim, abort) || !mbar_wait(&sf_full[s], par, lim, abort)) {
+        fail();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_base = smem_u32(sA + (size_t)s * a_bytes);
+      const uint32_t b_base = smem_u32(sB + (size_t)s * b_bytes);
+      const uint32_t sf_col = kSfCol0 + (uint32_t)s * (4 + 4 * p.nsub);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // four 32-K steps, scale byte j of each vector
+        for (int sub = 0; sub < p.nsub; ++sub) {
+          const uint32_t idesc = idesc_mxf8f6f4(a_fmt, 0u, (uint32_t)p.sub_n, (uint32_t)j, (uint32_t)j);
+          const uint64_t ad = smem_desc_sw128(a_base + 32 * j);
+          const uint64_t bd = smem_desc_sw128(b_base + (uint32_t)sub * p.sub_n * kBlockK + 32 * j);
+          mma_mxf8f6f4(tmem + (uint32_t)sub * p.sub_n, ad, bd, idesc, tmem + sf_col, tmem + sf_col + 4 + 4 * sub,
+                       (kt > 0 || j > 0) ? 1u : 0u);
+        }
+      }
+      tc_commit(&empty[s]);
+    }
+    tc_commit(acc_full);  // completes once every MMA issued above has finished
+    if (*abort) mbar_wait(acc_full, 0, kDrainLimit, nullptr);
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ scale vectors, then epilogue
+    const int q = warp - 4;  // tensor-memory lane quadrant of this warp
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    pdl_wait();
+    bool ok = true;
+    for (int kt = 0; kt < nk; ++kt) {
+      const int s = kt % S;
+      const uint32_t it = kt / S;
+      // lane 0 waits and the result is broadcast, so the warp stays converged for the
+      // .sync.aligned tensor-memory stores below
+      int got = 0;
+      if (lane == 0) got = mbar_wait(&empty[s], (it - 1) & 1, lim, abort);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) {
+        if (lane == 0) fail();
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sf_col = kSfCol0 + (uint32_t)s * (4 + 4 * p.nsub);
+      // weight scale vectors: one byte per 32-K step (4 per stage) for each of the 128 rows
+      uint32_t wa[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = (p.sf_layout == 0) ? (lane + 32 * j) : (32 * q + lane);
+        const int n = n0 + r;
+        uint32_t wv = 0x7F7F7F7Fu;
+        if (n < p.N) {
+          if (p.fp4) wv = __ldg(reinterpret_cast<const uint32_t*>(p.ws + (int64_t)n * p.lds + 4 * kt));
+          else wv = rep4(__ldg(p.ws + (int64_t)(n0 / 128) * p.lds + kt));
+        }
+        wa[j] = wv;
+      }
+      tmem_st_x4(tmem + lane_base + sf_col, wa[0], wa[1], wa[2], wa[3]);
+      // activation scale vectors: the token's 1x128 scale repeated for the 4 steps
+      for (int sub = 0; sub < p.nsub; ++sub) {
+        uint32_t wb[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = (p.sf_layout == 0) ? (lane + 32 * j) : (32 * q + lane);
+          const int t = t0 + sub * p.sub_n + r;
+          wb[j] = (r < p.sub_n && t < p.M) ? rep4(__ldg(p.as + (int64_t)t * p.las + kt)) : 0x7F7F7F7Fu;
+        }
+        tmem_st_x4(tmem + lane_base + sf_col + 4 + 4 * sub, wb[0], wb[1], wb[2], wb[3]);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sf_full[s]);
+    }
+    int got = 0;
+    if (ok && lane == 0) got = mbar_wait(acc_full, 0, lim, abort);
+    got = __shfl_sync(0xffffffffu, got, 0);
+    if (got) {
+      tc_fence_after();
+      const int n = n0 + 32 * q + lane;
+      const float bias = (p.bias && n < p.N) ? bf16_bits_to_f32(p.bias[n]) : 0.f;
+      for (int c0 = 0; c0 < p.tt; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_x32(tmem + lane_base + (uint32_t)c0, r);
+        tmem_wait_ld();
+        if (n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int t = t0 + c0 + j;
+            if (c0 + j < p.tt && t < p.M) {
+              uint16_t yb = f32_to_bf16_rn(__uint_as_float(r[j]));
+              if (p.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + bias);
+              p.y[(int64_t)t * p.ldy + n] = yb;
+            }
+          }
+        }
+      }
+    } else if (ok && lane == 0) {
+      fail();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) fprintf(stderr, "qlinear: cuTensorMapEncodeTiled failed (%d)\n", (int)r);
+  return r == CUDA_SUCCESS;
+}
+
+size_t act_q_bytes(int64_t M, int64_t K) { return (size_t)M * K; }
+size_t act_s_bytes(int64_t M, int64_t K) { return (size_t)M * (K / 128); }
+
+cudaError_t quantize_activations(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const GemmArgs& g,
+                                 uint8_t* aq_dbg, uint8_t* as_dbg, cudaStream_t st) {
+  return launch_quant_e4m3(x, (int)M, (int)K, ldx, g.aq, K, g.as, K / 128, 0, aq_dbg, as_dbg, st);
+}
+
+#ifndef QL_SF_LAYOUT
+#define QL_SF_LAYOUT 0
+#endif
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
+  TcParams p = {};
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.fp4 = g.fp4;
+  int mpad = ((g.M + 15) / 16) * 16;
+  if (mpad > 256) mpad = 256;
+  p.nsub = (mpad + 127) / 128;
+  p.sub_n = (((mpad + p.nsub - 1) / p.nsub) + 15) / 16 * 16;
+  p.tt = p.nsub * p.sub_n;
+  const size_t stage = (size_t)kBlockN * kBlockK + (size_t)p.tt * kBlockK;
+  const size_t budget = 227 * 1024 - 1024 - 256;
+  int S = (int)(budget / stage);
+  if (S > 8) S = 8;
+  p.stages = S;
+  p.ws = g.ws;
+  p.lds = g.lds;
+  p.as = g.as;
+  p.las = g.K / 128;
+  p.y = g.y;
+  p.ldy = g.ldy;
+  p.bias = g.bias;
+  p.status = g.status;
+  p.wait_limit = g.wait_limit;
+  p.sf_layout = QL_SF_LAYOUT;
+
+  CUtensorMap ta, tb;
+  const bool ok_a = g.fp4 ? make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w, (uint64_t)g.K, (uint64_t)g.N,
+                                     (uint64_t)g.ldw, kBlockK, kBlockN)
+                          : make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.w, (uint64_t)g.K, (uint64_t)g.N,
+                                     (uint64_t)g.ldw, kBlockK, kBlockN);
+  const bool ok_b = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.aq, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.K,
+                             kBlockK, (uint32_t)p.tt);
+  if (!ok_a || !ok_b) return cudaErrorInvalidValue;
+
+  const size_t smem = 1024 + (size_t)S * stage + (size_t)(3 * S + 1) * 8;
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((g.N + kBlockN - 1) / kBlockN), (unsigned)((g.M + p.tt - 1) / p.tt), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, ta, tb, p);
+}
+
+}  // namespace tc
+}  // namespace ql

@@ -1,0 +1,49 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "skinny.cuh"
+
+namespace ql {
+
+constexpr int kNumSMs = 152;  // GB300: 2 dies x 76 SMs (checked against the device at launch)
+
+// launch helpers (return the CUDA error of the launch)
+cudaError_t launch_quant_int8(const uint16_t* x, int M, int K, int64_t ldx, int8_t* xq, float* xs,
+                              int8_t* xq_dbg, float* xs_dbg, cudaStream_t st);
+cudaError_t launch_quant_e4m3(const uint16_t* x, int M, int K, int64_t ldx, uint8_t* q, int64_t ldq,
+                              uint8_t* s, int64_t lds, int s_transposed, uint8_t* q_dbg, uint8_t* s_dbg,
+                              cudaStream_t st);
+cudaError_t launch_skinny(int fmt, int mt, int epi, const SkinnyArgs& a, dim3 grid, cudaStream_t st, bool pdl);
+
+struct MoeRouteArgs {
+  const uint16_t* logits;
+  const int32_t* ids_in;
+  const float* w_in;
+  int M, E, topk, renorm;
+  int32_t* ids;
+  float* wts;
+  int32_t* offsets;
+  int32_t* pairs;
+  int32_t* uniq;
+  int32_t* nuniq;
+  int32_t* ids_dbg;
+  float* w_dbg;
+  uint32_t* status;
+};
+cudaError_t launch_moe_route(const MoeRouteArgs& r, cudaStream_t st);
+cudaError_t launch_moe_combine(const float* o, const int32_t* ids, const float* w, int M, int topk, int H,
+                               uint16_t* y, cudaStream_t st);
+
+// split-K choice of the skinny kernel (shared by the workspace query and the launch)
+struct SplitK {
+  int ks, kc;
+};
+SplitK skinny_split(int fmt, int mt, int64_t row_blocks, int64_t K);
+size_t skinny_smem(int fmt, int mt, int kc);
+
+uint32_t wait_limit();
+
+}  // namespace ql

@@ -1,0 +1,153 @@
+// MoE decode helpers: softmax top-k routing with grouped dispatch, and the weighted combine.
+//
+// Routing ([DSV4] §0.1, the M=1 routing fast path "Q1", and §0.3 grouped batch MoE): per token
+// p = softmax(logits) (evaluated in fp64, so the probabilities match an fp64 reference to the
+// last fp32 bit), the topk experts with the largest logits (equal logits: lower expert id
+// first), weights p[ids] (renormalised on request).  Dispatch groups the (token, slot) pairs
+// by expert with a stable counting sort and lists the distinct experts in first-use order;
+// the expert GEMMs launch one CTA column per distinct expert.
+#include "internal.h"
+
+namespace ql {
+
+constexpr int kRouteThreads = 512;  // one warp per token, M <= 16
+
+__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const MoeRouteArgs r) {
+  extern __shared__ float s_lg[];  // [M][E] logits (fp32, exact bf16 values)
+  __shared__ int s_ids[256];
+  __shared__ int s_cnt[1025];
+  const int M = r.M, E = r.E, topk = r.topk;
+  const int P = M * topk;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* taken = reinterpret_cast<uint8_t*>(s_lg + (size_t)M * E);  // [M][E]
+
+  if (r.logits) {
+    if (warp < M) {
+      const int m = warp;
+      float mx = -INFINITY;
+      for (int e = lane; e < E; e += 32) {
+        const float v = bf16_bits_to_f32(r.logits[(int64_t)m * E + e]);
+        s_lg[m * E + e] = v;
+        taken[m * E + e] = 0;
+        mx = fmaxf(mx, v);
+      }
+      mx = warp_max(mx);
+      double sum = 0.0;
+      for (int e = lane; e < E; e += 32) sum += exp((double)s_lg[m * E + e] - (double)mx);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      double wsum = 0.0;
+      double pw[16];
+      for (int j = 0; j < topk; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+        for (int e = lane; e < E; e += 32) {
+          if (taken[m * E + e]) continue;
+          const float v = s_lg[m * E + e];
+          if (v > bv || (v == bv && e < be)) { bv = v; be = e; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        }
+        __syncwarp();
+        if (lane == 0) taken[m * E + be] = 1;
+        __syncwarp();
+        const double p = exp((double)bv - (double)mx) / sum;
+        pw[j] = p;
+        wsum += p;
+        if (lane == 0) {
+          s_ids[m * topk + j] = be;
+          r.ids[m * topk + j] = be;
+        }
+      }
+      if (lane == 0) {
+        for (int j = 0; j < topk; ++j) {
+          const float w = (float)(r.renorm ? pw[j] / wsum : pw[j]);
+          r.wts[m * topk + j] = w;
+          if (r.w_dbg) r.w_dbg[m * topk + j] = w;
+          if (r.ids_dbg) r.ids_dbg[m * topk + j] = s_ids[m * topk + j];
+        }
+      }
+    }
+  } else {
+    for (int p = threadIdx.x; p < P; p += blockDim.x) {
+      int e = r.ids_in[p];
+      if (e < 0 || e >= E) {
+        raise_flag(r.status, 2u);
+        e = -1;
+      }
+      s_ids[p] = e;
+      r.ids[p] = e;
+      r.wts[p] = r.w_in[p];
+      if (r.ids_dbg) r.ids_dbg[p] = e;
+      if (r.w_dbg) r.w_dbg[p] = r.w_in[p];
+    }
+  }
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // stable counting sort of the pairs by expert; distinct experts in first-use order
+    for (int p = 0; p < P; ++p)
+      if (s_ids[p] >= 0) s_cnt[s_ids[p]]++;
+    int run = 0, nu = 0;
+    for (int e = 0; e < E; ++e) {
+      const int c = s_cnt[e];
+      r.offsets[e] = run;
+      s_cnt[e] = run;
+      run += c;
+    }
+    r.offsets[E] = run;
+    for (int p = 0; p < P; ++p) {
+      const int e = s_ids[p];
+      if (e < 0) continue;
+      if (r.offsets[e] == s_cnt[e]) r.uniq[nu++] = e;  // first pair of this expert
+      r.pairs[s_cnt[e]++] = p;
+    }
+    *r.nuniq = nu;
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+}
+
+cudaError_t launch_moe_route(const MoeRouteArgs& r, cudaStream_t st) {
+  const size_t smem = r.logits ? (size_t)r.M * r.E * 5 : 0;
+  cudaError_t err = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  moe_route_kernel<<<1, kRouteThreads, smem, st>>>(r);
+  return cudaGetLastError();
+}
+
+// y[m, n] = bf16( sum_j w[m,j] * o[m*topk + j, n] ), summed in slot order
+__global__ void __launch_bounds__(256) moe_combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ ids,
+                                                          const float* __restrict__ w, int topk, int H,
+                                                          uint16_t* __restrict__ y) {
+  pdl_wait();
+  const int m = blockIdx.y;
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= H) return;
+  float acc = 0.f;
+  for (int j = 0; j < topk; ++j) {
+    const int p = m * topk + j;
+    if (ids[p] >= 0) acc = fmaf(w[p], o[(int64_t)p * H + n], acc);
+  }
+  y[(int64_t)m * H + n] = f32_to_bf16_rn(acc);
+}
+
+cudaError_t launch_moe_combine(const float* o, const int32_t* ids, const float* w, int M, int topk, int H,
+                               uint16_t* y, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((H + 255) / 256, M, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, moe_combine_kernel, o, ids, w, topk, H, y);
+}
+
+}  // namespace ql

@@ -1,0 +1,82 @@
+"""INT8 W8A8 parity: CUDA path vs the oracle on identical seeded inputs.
+Bit-exact: x_q, x_s, int32 accumulators.  y within 1e-3*sum|w x| + 1 bf16 ulp."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from _util import bits_of, check_float, gpu_lib, sample_rows, to_bf16_tensor
+from oracle import qlinear_oracle as Q
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ql():
+    return gpu_lib()
+
+
+def run(ql, c, bias=None, wsl=None):
+    x = to_bf16_tensor(c["x"])
+    w = torch.from_numpy(c["w"]).cuda()
+    ws = torch.from_numpy(c["w_s"] if wsl is None else c["w_s"][:wsl]).cuda()
+    b = None if bias is None else to_bf16_tensor(bias)
+    y, acc, xq, xs, path = ql.qlinear_int8_w8a8(x, w, ws, b, debug=True)
+    torch.cuda.synchronize()
+    assert path == "int8_skinny"
+    return bits_of(y), acc.cpu().numpy(), xq.cpu().numpy(), xs.cpu().numpy()
+
+
+def compare(c, got, rows=None, bias=None, wsl=None):
+    y, acc, xq, xs = got
+    K = c["x"].shape[1]
+    ref = Q.int8_w8a8(c["x"], c["w"][:, :K], c["w_s"] if wsl is None else c["w_s"][:wsl], bias, rows=rows)
+    assert np.array_equal(xq, ref["x_q"]), "x_q differs"
+    assert np.array_equal(xs.view(np.uint32), ref["x_s"].view(np.uint32)), "x_s differs"
+    sl = slice(None) if rows is None else rows
+    assert np.array_equal(acc[:, sl], ref["acc"]), "int32 accumulators differ"
+    y_ref = ref["y"]
+    from oracle import formats as F
+    check_float(y[:, sl], F.bf16_to_f64(y_ref), ref["abs_sum"] + 0.0)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 512, 1024), (3, 200, 304), (16, 1000, 2048), (9, 130, 4096),
+                                   (5, 77, 16), (8, 64, 17408), (2, 4097, 640)])
+def test_int8_small(ql, M, N, K):
+    c = synth.int8_case(M, N, K, seed=M + N)
+    compare(c, run(ql, c))
+
+
+def test_int8_many_tokens_chunked(ql):
+    c = synth.int8_case(37, 96, 512, seed=3)
+    compare(c, run(ql, c))
+
+
+def test_int8_bias_per_tensor_scale_padded_rows(ql):
+    c = synth.int8_case(4, 150, 256, seed=11, ldw=320)
+    bias = synth.bf16_normal(synth.rng(11, 99), (150,))
+    compare(c, run(ql, c, bias=bias, wsl=1), bias=bias, wsl=1)
+
+
+def test_int8_zero_token_and_large_values(ql):
+    c = synth.int8_case(3, 128, 256, seed=12)
+    c["x"][1] = 0
+    c["x"][2] = synth.f32_to_bf16_bits(np.linspace(-3e4, 3e4, 256).astype(np.float32))
+    got = run(ql, c)
+    assert got[3][1] == 0 and not got[2][1].any() and not got[0][1].any()
+    compare(c, got)
+
+
+def test_int8_repeat_is_deterministic(ql):
+    c = synth.int8_case(16, 5120, 17408 // 4, seed=13)
+    a = run(ql, c)
+    b = run(ql, c)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408), (10240, 5120)])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
+def test_int8_full_size_sampled(ql, N, K, M):
+    c = synth.int8_case(M, N, K, seed=0)
+    rows = sample_rows(N, seed=M)
+    compare(c, run(ql, c), rows=rows)
