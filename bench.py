@@ -1,0 +1,600 @@
+"""Benchmark of the quantized decode linear layer on GB300.
+
+Default workload: INT8 W8A8 skinny GEMM at the 27B-class decode shapes
+(N,K) in {(17408,5120), (5120,17408), (10240,5120)} x M in {1,2,4,8,16} tokens.
+One step = one call of each of those 15 (shape, M) cases (per-token INT8 activation
+quantisation + skinny GEMM each).  Metric: achieved HBM GB/s = algorithmic bytes
+(weights + weight scales + activations + outputs) / device time, plus µs per call.
+
+Weights rotate over 6 copies per shape (>= 1 GB in total), so every call streams its
+weights from HBM (no call finds them in the 129 MB L2).  Activations are small and stay
+wherever the previous write left them, as in a decode step.
+
+--config selects the other workloads (c0: INT8 M=1 N=512 K=1024; c2: FP8 128x128 block;
+c3: MXFP4 MoE E=256 H=4096 I=2048 top-8; c4: tcgen05 FP8/MXFP4 M=64..256).
+--impl reference times the CPU oracle on a bounded row sample of the same workload.
+Under torchrun each rank runs an independent replica (the layer needs no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "µs/call and achieved HBM GB/s (% of GB300 roofline) for quantized decode GEMV"
+C1_SHAPES = [(17408, 5120), (5120, 17408), (10240, 5120)]
+C1_MS = [1, 2, 4, 8, 16]
+C2_SHAPES = [(17408, 5120), (5120, 17408)]
+C2_MS = [1, 4, 8, 16]
+C3_MS = list(range(1, 10))
+C4_MS = [64, 128, 256]
+ROTATE = 6  # weight copies per shape (>= 3 x 44.6 MB between reuses)
+
+
+# ----------------------------------------------------------------------------- bytes / flops
+def bytes_int8(M, N, K):
+    return N * K + 4 * N + 2 * M * K + 2 * M * N
+
+
+def bytes_fp8(M, N, K):
+    return N * K + (-(-N // 128)) * (-(-K // 128)) + 2 * M * K + 2 * M * N
+
+
+def bytes_mxfp4(M, N, K):
+    return N * K // 2 + N * K // 32 + 2 * M * K + 2 * M * N
+
+
+def bytes_moe_expert(H, I):
+    return 2 * I * H // 2 + 2 * I * H // 32 + H * I // 2 + H * I // 32
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha1()
+    for f in ("skinny.cuh", "kernels_skinny.cu", "kernels_quant.cu", "kernels_moe.cu", "gemm_tcgen05.cu", "tc_ptx.cuh",
+              "common.cuh"):
+        h.update(open(os.path.join(ROOT, "skinny_gemm_dequant_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:12]
+
+
+def load_traffic(config):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None if
+    the summary is missing or the kernels changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(config)
+    if not d or d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads (GPU)
+class Workload:
+    """A list of calls; each call(i) enqueues one layer call on the current stream."""
+
+    def __init__(self, name, calls, launches_per_step, cfg):
+        self.name, self.calls, self.launches_per_step, self.cfg = name, calls, launches_per_step, cfg
+
+    @property
+    def bytes_per_step(self):
+        return sum(c["bytes"] for c in self.calls)
+
+
+def dev_bf16(bits, torch):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def build_c1(ql, torch, shapes=C1_SHAPES, Ms=C1_MS, name="c1"):
+    calls = []
+    weights = {}
+    for (N, K) in shapes:
+        c = synth.int8_case(1, N, K, seed=0)
+        w0 = torch.from_numpy(c["w"]).cuda()
+        weights[(N, K)] = ([w0] + [w0.clone() for _ in range(ROTATE - 1)], torch.from_numpy(c["w_s"]).cuda(),
+                           {"i": 0})
+    for M in Ms:  # shapes inner; each use of a shape takes the next weight copy
+        for (N, K) in shapes:
+            ws, sc, state = weights[(N, K)]
+            x = dev_bf16(synth.int8_case(M, 1, K, seed=1)["x"], torch)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+
+            def call(ws=ws, sc=sc, x=x, y=y, state=state):
+                w = ws[state["i"] % ROTATE]
+                state["i"] += 1
+                ql.qlinear_int8_w8a8(x, w, sc, out=y)
+
+            calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": bytes_int8(M, N, K), "flops": 2 * M * N * K,
+                          "x": x, "y": y, "kind": "int8"})
+    cfg = {"workload": "INT8 W8A8 skinny GEMM, 27B-class decode shapes (N,K) in "
+                       "{(17408,5120),(5120,17408),(10240,5120)} x M in {1,2,4,8,16}",
+           "shapes": [list(s) for s in shapes], "M": Ms}
+    return Workload(name, calls, 2 * len(calls), cfg)
+
+
+def build_c0(ql, torch):
+    w = build_c1(ql, torch, shapes=[(512, 1024)], Ms=[1], name="c0")
+    w.cfg = {"workload": "INT8 W8A8 GEMV M=1 N=512 K=1024", "shapes": [[512, 1024]], "M": [1]}
+    return w
+
+
+def build_c2(ql, torch):
+    calls = []
+    weights = {}
+    for (N, K) in C2_SHAPES:
+        c = synth.fp8_block_case(1, N, K, seed=0)
+        w0 = torch.from_numpy(c["w"]).cuda()
+        weights[(N, K)] = ([w0] + [w0.clone() for _ in range(ROTATE - 1)], torch.from_numpy(c["s"]).cuda(),
+                           {"i": 0})
+    for M in C2_MS:
+        for (N, K) in C2_SHAPES:
+            ws, sc, state = weights[(N, K)]
+            x = dev_bf16(synth.fp8_block_case(M, 1, K, seed=1)["x"], torch)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+
+            def call(ws=ws, sc=sc, x=x, y=y, state=state):
+                w = ws[state["i"] % ROTATE]
+                state["i"] += 1
+                ql.qlinear_fp8_block(x, w, sc, out=y)
+
+            calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": bytes_fp8(M, N, K), "flops": 2 * M * N * K,
+                          "x": x, "y": y, "kind": "fp8"})
+    cfg = {"workload": "FP8 E4M3 128x128 UE8M0 block-scaled GEMV, bf16 activations, (N,K) in "
+                       "{(17408,5120),(5120,17408)} x M in {1,4,8,16}"}
+    return Workload("c2", calls, len(calls), cfg)
+
+
+def build_c3(ql, torch):
+    from oracle import qlinear_oracle as Q  # only to count the experts each routing touches
+    E, H, I, topk = 256, 4096, 2048, 8
+    w = synth.moe_weights_only(E, H, I, seed=0)
+    dev = [torch.from_numpy(w[k]).cuda() for k in ("w13", "s13", "w2", "s2")]
+    calls = []
+    for M in C3_MS:
+        sets = []
+        for r in range(ROTATE):  # different routings per rotation: different experts, cold L2
+            t = synth.moe_tokens(M, E, H, seed=100 + 10 * M + r)
+            ids, _ = Q.route_topk(t["logits"], topk)
+            sets.append((dev_bf16(t["x"], torch), dev_bf16(t["logits"], torch), len(np.unique(ids))))
+        y = torch.empty(M, H, dtype=torch.bfloat16, device="cuda")
+        state = {"i": 0}
+
+        def call(sets=sets, y=y, state=state):
+            x, lg, _ = sets[state["i"] % ROTATE]
+            state["i"] += 1
+            ql.moe_mxfp4_grouped(x, *dev, router_logits=lg, topk=topk, out=y)
+
+        uniq = float(np.mean([s[2] for s in sets]))
+        b = uniq * bytes_moe_expert(H, I) + 2 * M * H * 2 + 2 * M * E
+        calls.append({"fn": call, "M": M, "N": H, "K": I, "bytes": b, "flops": 2 * M * topk * 3 * H * I,
+                      "x": sets[0][0], "y": y, "kind": "moe", "unique_experts": uniq})
+    cfg = {"workload": "MXFP4 MoE decode: 256 experts, hidden 4096, intermediate 2048, top-8, M in 1..9",
+           "bytes": "unique touched experts x 13369344 B + x + logits + y"}
+    return Workload("c3", calls, 4 * len(calls), cfg)
+
+
+def build_c4(ql, torch):
+    calls = []
+    N, K = 17408, 5120
+    cf = synth.fp8_block_case(1, N, K, seed=0)
+    cm = synth.mxfp4_dense_case(1, N, K, seed=0)
+    lds = -(-(K // 32) // 16) * 16
+    sm = np.zeros((N, lds), np.uint8)
+    sm[:, : K // 32] = cm["s"]
+    fw = torch.from_numpy(cf["w"]).cuda()
+    mw = torch.from_numpy(cm["w"]).cuda()
+    fws = [fw] + [fw.clone() for _ in range(ROTATE - 1)]
+    mws = [mw] + [mw.clone() for _ in range(ROTATE - 1)]
+    fs = torch.from_numpy(cf["s"]).cuda()
+    ms = torch.from_numpy(sm).cuda()
+    rot = {"fp8": {"i": 0}, "mxfp4": {"i": 0}}
+    for M in C4_MS:
+        x = dev_bf16(synth.fp8_block_case(M, 1, K, seed=1)["x"], torch)
+        for kind in ("fp8", "mxfp4"):
+            y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+            state = rot[kind]
+            if kind == "fp8":
+                def call(x=x, y=y, state=state):
+                    w = fws[state["i"] % ROTATE]
+                    state["i"] += 1
+                    ql.qlinear_fp8_block(x, w, fs, act_mode=ql.ACT_E4M3_1X128, out=y)
+                b = bytes_fp8(M, N, K)
+            else:
+                def call(x=x, y=y, state=state):
+                    w = mws[state["i"] % ROTATE]
+                    state["i"] += 1
+                    ql.qlinear_mxfp4(x, w, ms, act_mode=ql.ACT_E4M3_1X128, out=y)
+                b = bytes_mxfp4(M, N, K)
+            calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": b, "flops": 2 * M * N * K, "x": x, "y": y,
+                          "kind": kind + "_tcgen05"})
+    cfg = {"workload": "tcgen05 block-scaled GEMM, 1x128 E4M3 activations, FP8 128x128 and MXFP4 weights, "
+                       "(N,K)=(17408,5120), M in {64,128,256}"}
+    return Workload("c4", calls, 2 * len(calls), cfg)
+
+
+BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4": build_c4}
+
+
+# ----------------------------------------------------------------------------- timing
+def capture(torch, body):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        body()
+    return g
+
+
+def step_graphs(wl, torch):
+    """ROTATE graphs of one step each, captured in order: replaying them cyclically keeps every
+    use of a weight set on a different copy than the previous use."""
+    def body():
+        for c in wl.calls:
+            c["fn"]()
+    return [capture(torch, body) for _ in range(ROTATE)]
+
+
+def time_steps(graphs, steps, torch):
+    st = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for i in range(steps):
+        graphs[i % len(graphs)].replay()
+    b.record(st)
+    b.synchronize()
+    return a.elapsed_time(b)  # ms
+
+
+def time_per_call(wl, torch, uses=32, reps=8):
+    """µs per call: a graph of `uses` back-to-back calls of one case (rotating weight copies),
+    replayed `reps` times between two events."""
+    st = torch.cuda.current_stream()
+    out = []
+    for c in wl.calls:
+        def body(c=c):
+            for _ in range(uses):
+                c["fn"]()
+        g = capture(torch, body)
+        g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(reps):
+            g.replay()
+        b.record(st)
+        b.synchronize()
+        out.append(a.elapsed_time(b) * 1e3 / (uses * reps))
+        del g
+    return out
+
+
+def time_e2e(wl, steps, torch):
+    """Through the public API with host buffers: each call copies its activations from pinned
+    host memory, runs, and copies its output back to pinned host memory, all inside the timed
+    region (the step's calls and copies captured in CUDA graphs, replayed)."""
+    st = torch.cuda.current_stream()
+    hx = [c["x"].cpu().pin_memory() for c in wl.calls]
+    hy = [torch.empty(c["y"].shape, dtype=c["y"].dtype).pin_memory() for c in wl.calls]
+
+    def body():
+        for i, c in enumerate(wl.calls):
+            c["x"].copy_(hx[i], non_blocking=True)
+            c["fn"]()
+            hy[i].copy_(c["y"], non_blocking=True)
+    graphs = [capture(torch, body) for _ in range(ROTATE)]
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for i in range(steps):
+        graphs[i % len(graphs)].replay()
+    b.record(st)
+    b.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in hx)
+    d2h = sum(t.numel() * t.element_size() for t in hy)
+    return a.elapsed_time(b), h2d, d2h
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+_CASES = {}
+
+
+def _case(key, fn):
+    if key not in _CASES:
+        _CASES[key] = fn()
+    return _CASES[key]
+
+
+def oracle_sample(config, rows_per_call):
+    """Time the oracle (as it stands) on a bounded row sample of the workload; returns
+    (seconds spent in the oracle, algorithmic bytes of the sampled work, description).
+    Input generation is outside the timed part."""
+    from oracle import formats as F
+    from oracle import qlinear_oracle as Q
+    sec = 0.0
+    done = 0.0
+    if config in ("c0", "c1"):
+        shapes, Ms = ([(512, 1024)], [1]) if config == "c0" else (C1_SHAPES, C1_MS)
+        for (N, K) in shapes:
+            c = _case(("int8", N, K), lambda: synth.int8_case(16, N, K, seed=0))
+            rows = np.arange(min(rows_per_call, N))
+            for M in Ms:
+                t = time.perf_counter()
+                Q.int8_w8a8(c["x"][:M], c["w"], c["w_s"], rows=rows)
+                sec += time.perf_counter() - t
+                done += bytes_int8(M, len(rows), K)
+        desc = f"INT8 oracle on the first {rows_per_call} output rows of each of the {len(shapes) * len(Ms)} calls"
+    elif config == "c2":
+        for (N, K) in C2_SHAPES:
+            c = _case(("fp8", N, K), lambda: synth.fp8_block_case(16, N, K, seed=0))
+            rows = np.arange(min(rows_per_call, N))
+            for M in C2_MS:
+                t = time.perf_counter()
+                Q.fp8_block(F.bf16_to_f64(c["x"][:M]), c["w"], c["s"], K, rows=rows)
+                sec += time.perf_counter() - t
+                done += bytes_fp8(M, len(rows), K)
+        desc = f"FP8 block oracle on the first {rows_per_call} output rows of each of the 8 calls"
+    elif config == "c3":
+        E, H, I = 256, 4096, 2048
+        wsub = _case(("moe8",), lambda: synth.moe_weights_only(8, H, I, seed=0))
+        for M in (1, 9):
+            tk = _case(("tok", M), lambda: synth.moe_tokens(M, E, H, seed=0))
+            cols = np.arange(min(rows_per_call, I))
+            t = time.perf_counter()
+            ids, _ = Q.route_topk(tk["logits"], 8)
+            ids = np.asarray(ids) % 8  # 8 stand-in experts carry the sampled work
+            Q.moe_gate_up(tk["x"], ids, wsub["w13"], wsub["s13"], I, cols=cols)
+            sec += time.perf_counter() - t
+            done += len(np.unique(ids)) * 2 * len(cols) * (H // 2 + H // 32)
+        desc = f"MoE oracle routing + gate_up on {rows_per_call} intermediate rows for M=1 and M=9"
+    else:
+        N, K = 17408, 5120
+        c = _case(("fp8", N, K, 64), lambda: synth.fp8_block_case(64, N, K, seed=0))
+        rows = np.arange(min(rows_per_call, N))
+        t = time.perf_counter()
+        Q.fp8_block_act_quant(c["x"], c["w"], c["s"], K, rows=rows)
+        sec += time.perf_counter() - t
+        done += bytes_fp8(64, len(rows), K)
+        desc = f"FP8 1x128-activation oracle on {rows_per_call} rows at M=64"
+    return sec, done, desc
+
+
+def cpu_baseline(config, budget_s=15.0):
+    """Oracle throughput in the metric's unit on a bounded sample, single threaded."""
+    rows = 64
+    sec, b, desc = oracle_sample(config, rows)
+    # grow the sample until it takes a few seconds, within the budget
+    while sec < budget_s / 4 and rows < 4096:
+        rows *= 4
+        sec, b, desc = oracle_sample(config, rows)
+    return {"value": b / sec / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc,
+            "seconds": round(sec, 3)}
+
+
+# ----------------------------------------------------------------------------- main
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(values, op="max"):
+    return max(values) if op == "max" else sum(values)
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    # the oracle is single threaded numpy (integer matmul and fp64 per-block matmuls)
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    rows = 8
+    for _ in range(args.warmup):
+        oracle_sample(args.config, rows)
+    t = 0.0
+    b = 0.0
+    for _ in range(args.steps):
+        s, bb, desc = oracle_sample(args.config, rows)
+        t += s
+        b += bb
+    val = b / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic", "config": {"workload": BUILD_CFG_NAMES[args.config]},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": desc + f" ({rows} rows per call per step)"},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+BUILD_CFG_NAMES = {
+    "c0": "INT8 W8A8 GEMV M=1 N=512 K=1024",
+    "c1": "INT8 W8A8 skinny GEMM, 27B-class decode shapes (N,K) in {(17408,5120),(5120,17408),(10240,5120)} "
+          "x M in {1,2,4,8,16}",
+    "c2": "FP8 E4M3 128x128 block-scaled GEMV (17408,5120),(5120,17408) x M in {1,4,8,16}",
+    "c3": "MXFP4 MoE decode E=256 H=4096 I=2048 top-8, M in 1..9",
+    "c4": "tcgen05 block-scaled GEMM FP8/MXFP4, (17408,5120), M in {64,128,256}",
+}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c1", choices=sorted(BUILDERS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true", help="a few steps, no clocks/e2e/baseline (for ncu)")
+    args = ap.parse_args()
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        if args.steps is None:
+            args.steps = 20
+        return run_reference(args, ws, rank)
+
+    import torch
+    if args.steps is None:
+        args.steps = {"c0": 20000, "c1": 4000, "c2": 4000, "c3": 2000, "c4": 2000}[args.config]
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    import skinny_gemm_dequant_gb300 as ql
+    wl = BUILDERS[args.config](ql, torch)
+    for c in wl.calls:  # sizes the shared workspace before any capture
+        c["fn"]()
+    torch.cuda.synchronize()
+    if args.profile:  # plain launches, no graphs (for ncu launch lists)
+        for _ in range(args.warmup + args.steps):
+            for c in wl.calls:
+                c["fn"]()
+        torch.cuda.synchronize()
+        return
+    graphs = step_graphs(wl, torch)
+    for i in range(max(args.warmup, 3)):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms_total = time_steps(graphs, args.steps, torch)
+    torch.cuda.synchronize()
+    if pg:
+        t = torch.tensor([ms_total], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    peaks = load_peaks()
+    value = ws * wl.bytes_per_step / (ms_step * 1e-3) / 1e9  # GB/s, all ranks
+
+    per_call = time_per_call(wl, torch)
+    calls = []
+    for c, us in zip(wl.calls, per_call):
+        gbs = c["bytes"] / (us * 1e-6) / 1e9
+        e = {"kind": c["kind"], "M": c["M"], "N": c["N"], "K": c["K"], "us": round(us, 3), "GBps": round(gbs, 1),
+             "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)}
+        if "unique_experts" in c:
+            e["unique_experts"] = c["unique_experts"]
+        calls.append(e)
+    tot_b = sum(c["bytes"] for c in wl.calls)
+    tot_us = sum(per_call)
+    achieved = tot_b / (tot_us * 1e-6) / 1e9
+    traffic = load_traffic(args.config)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)",
+                "kernel": "per-call layer kernels (activation quant + weight-streaming GEMM), bytes per call / "
+                          "event time per call, aggregated over the step's calls",
+                "algorithmic_bytes_per_step": tot_b}
+    if args.config == "c4":
+        fl = sum(c["flops"] for c in wl.calls)
+        roofline["tensor_tflops"] = round(fl / (tot_us * 1e-6) / 1e12, 1)
+
+    e2e_steps = max(3, min(args.steps // 10, 400))
+    e2e_ms, h2d, d2h = time_e2e(wl, e2e_steps, torch)
+    e2e_val = ws * wl.bytes_per_step / (e2e_ms / e2e_steps * 1e-3) / 1e9
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": {"c0": "int8", "c1": "int8", "c2": "fp8", "c3": "fp4", "c4": "fp8/fp4"}[
+                args.config], "data": "synthetic",
+            "config": dict(wl.cfg, parallelism=f"replicas x{ws}", l2="weights rotate over 6 copies per shape "
+                                                                   "(inputs larger than L2)"),
+            "us_per_call_mean": round(ms_step * 1e3 / len(wl.calls), 3),
+            "calls": calls, "roofline": roofline,
+            "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": wl.launches_per_step * args.steps,
+            "clocks": clk.summary()}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

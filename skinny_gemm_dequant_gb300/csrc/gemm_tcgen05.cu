@@ -20,6 +20,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdio>
+#include <atomic>
 #include <mutex>
 
 #include "gemm_tcgen05.h"
@@ -324,8 +325,12 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   if (!ok_a || !ok_b) return cudaErrorInvalidValue;
 
   const size_t smem = 1024 + (size_t)S * stage + (size_t)(3 * S + 1) * 8;
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  static std::atomic<int> attr_set{0};
+  if (!attr_set.load()) {
+    cudaError_t e = raise_smem_limit(tc_gemm_kernel);
+    if (e != cudaSuccess) return e;
+    attr_set.store(1);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((g.N + kBlockN - 1) / kBlockN), (unsigned)((g.M + p.tt - 1) / p.tt), 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

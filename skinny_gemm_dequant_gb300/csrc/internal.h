@@ -46,4 +46,19 @@ size_t skinny_smem(int fmt, int mt, int kc);
 
 uint32_t wait_limit();
 
+// Raise a kernel's dynamic shared-memory limit to the device's opt-in maximum minus its static
+// shared memory.  Done once per kernel, before any launch, so calls made during CUDA-graph
+// capture only enqueue work.
+template <class F>
+cudaError_t raise_smem_limit(F* kfn) {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kfn);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+  return e;
+}
+
 }  // namespace ql

@@ -6,6 +6,8 @@
 // first), weights p[ids] (renormalised on request).  Dispatch groups the (token, slot) pairs
 // by expert with a stable counting sort and lists the distinct experts in first-use order;
 // the expert GEMMs launch one CTA column per distinct expert.
+#include <atomic>
+
 #include "internal.h"
 
 namespace ql {
@@ -114,8 +116,12 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const MoeRoute
 
 cudaError_t launch_moe_route(const MoeRouteArgs& r, cudaStream_t st) {
   const size_t smem = r.logits ? (size_t)r.M * r.E * 5 : 0;
-  cudaError_t err = cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
+  static std::atomic<int> attr_set{0};
+  if (!attr_set.load()) {
+    cudaError_t err = raise_smem_limit(moe_route_kernel);
+    if (err != cudaSuccess) return err;
+    attr_set.store(1);
+  }
   moe_route_kernel<<<1, kRouteThreads, smem, st>>>(r);
   return cudaGetLastError();
 }

@@ -1,4 +1,6 @@
 // Instantiations and launch of the skinny weight-streaming GEMM (see skinny.cuh).
+#include <atomic>
+
 #include "internal.h"
 
 namespace ql {
@@ -37,8 +39,14 @@ template <int FMT, int MT, int EPI>
 static cudaError_t launch_one(const SkinnyArgs& a, dim3 grid, cudaStream_t st, bool pdl) {
   auto kfn = skinny_gemm_kernel<FMT, MT, EPI>;
   const size_t smem = skinny_smem_bytes<FMT, MT>(a.kc);
-  cudaError_t err = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
+  // raise the dynamic shared-memory limit once (to the largest size seen), so that calls made
+  // during CUDA-graph capture only enqueue the launch
+  static std::atomic<int> attr_set{0};
+  if (!attr_set.load()) {
+    cudaError_t err = raise_smem_limit(kfn);
+    if (err != cudaSuccess) return err;
+    attr_set.store(1);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(SK_THREADS, 1, 1);
