@@ -5,6 +5,7 @@
 
 #include "gemm_tcgen05.h"
 #include "internal.h"
+#include "skinny2.cuh"
 
 using namespace ql;
 
@@ -74,6 +75,49 @@ DenseLayout dense_layout(int fmt, int64_t M, int64_t N, int64_t K) {
   return l;
 }
 
+struct Dense2Layout {
+  Skinny2Plan p;
+  size_t x16, sc, part, total;
+};
+
+Dense2Layout dense2_layout(int fmt, int64_t Mc, int64_t N, int64_t K, int block_n) {
+  Dense2Layout l;
+  l.p = skinny2_plan(fmt, Mc, N, K, block_n);
+  Carver c;
+  l.x16 = c.take((size_t)kXCopies * l.p.mp * K * 2);
+  l.sc = c.take(16 * 4);
+  l.part = c.take((size_t)l.p.nb * l.p.maxseg * 16 * S2_ROWS * 4);
+  l.total = c.off;
+  return l;
+}
+
+// MXFP4 weights go through the persistent kernel when whole 256-K units and 8-byte scale
+// rows allow it; other shapes use the register-streaming kernel.
+bool mxfp4_v2_ok(int64_t K, int64_t lds, const void* wsb) {
+  return K % 256 == 0 && lds % 8 == 0 && (reinterpret_cast<uintptr_t>(wsb) & 7) == 0;
+}
+
+struct Dense2Call {
+  int fmt;
+  const uint16_t* x;
+  int64_t M, K, ldx;
+  const uint8_t* w;
+  int64_t N, ldw;
+  const uint8_t* wsb;
+  int64_t lds;
+  int block_n, block_k;
+  const float* w_scale;
+  int64_t w_scale_len;
+  const uint16_t* bias;
+  uint16_t* y;
+  int64_t ldy;
+  int32_t* acc_out;
+  int8_t* xq_out;
+  float* xs_out;
+};
+
+ql_status run_dense2(const Dense2Call& d, void* workspace, cudaStream_t st);
+
 struct MoeLayout {
   size_t ids, wts, offsets, pairs, uniq, nuniq, h, o, cnt_gu, part_gu, cnt_dn, part_dn, total;
   int mt, umax;
@@ -121,6 +165,47 @@ bool tc_path(int act_mode) { return act_mode == QL_ACT_E4M3_1X128; }
 
 uint32_t ql::wait_limit() { return g_wait_limit; }
 
+namespace {
+ql_status run_dense2(const Dense2Call& d, void* workspace, cudaStream_t st) {
+  for (int64_t m0 = 0; m0 < d.M; m0 += 16) {
+    const int64_t Mc = (d.M - m0) < 16 ? (d.M - m0) : 16;
+    const Dense2Layout l = dense2_layout(d.fmt, Mc, d.N, d.K, d.block_n);
+    uint16_t* x16 = at<uint16_t>(workspace, l.x16);
+    float* sc = at<float>(workspace, l.sc);
+    cudaError_t e;
+    if (d.fmt == FMT_INT8)
+      e = launch_prologue_int8(d.x + m0 * d.ldx, (int)Mc, l.p.mp, (int)d.K, d.ldx, x16, sc,
+                               d.xq_out ? d.xq_out + m0 * d.K : nullptr, d.xs_out ? d.xs_out + m0 : nullptr, st);
+    else
+      e = launch_prologue_bf16(d.x + m0 * d.ldx, (int)Mc, l.p.mp, (int)d.K, d.ldx, x16, sc, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    Skinny2Args a = {};
+    a.M = (int)Mc;
+    a.N = (int)d.N;
+    a.K = (int)d.K;
+    a.wsb = d.wsb;
+    a.lds = d.lds;
+    a.block_n = d.block_n;
+    a.block_k = d.block_k;
+    a.w_scale = d.w_scale;
+    a.w_scale_len = (int)d.w_scale_len;
+    a.x_s = sc;
+    a.tokscale = sc;
+    a.y = d.y + m0 * d.ldy;
+    a.ldy = d.ldy;
+    a.bias = d.bias;
+    a.acc_out = d.acc_out ? d.acc_out + m0 * d.N : nullptr;
+    a.part = at<float>(workspace, l.part);
+    a.tickets = at<unsigned>(workspace, kTicketOff);
+    a.status = at<uint32_t>(workspace, 0);
+    a.wait_limit = g_wait_limit;
+    e = launch_skinny2(d.fmt, l.p, a, d.w, d.ldw, x16, st);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return QL_OK;
+}
+}  // namespace
+
 extern "C" {
 
 const char* ql_status_string(ql_status s) {
@@ -144,22 +229,18 @@ size_t ql_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int to
   if (M < 0 || N < 0 || K < 0) return 0;
   const int64_t Mc = M < 16 ? M : 16;  // skinny kernels run 16 tokens at a time
   switch (op) {
-    case QL_OP_INT8_W8A8: {
-      DenseLayout l = dense_layout(FMT_INT8, Mc, N, K);
-      // the quantised activations of all M tokens live in the workspace
-      Carver c;
-      c.off = l.total;
-      c.take((size_t)M * K);
-      c.take((size_t)M * 4);
-      return c.off;
-    }
+    case QL_OP_INT8_W8A8:
+      return dense2_layout(FMT_INT8, Mc, N, K, 128).total;
     case QL_OP_FP8_BLOCK: {
-      const size_t a = dense_layout(FMT_FP8, Mc, N, K).total;
+      // block_n is not known here: 16 (the smallest accepted) bounds the scale staging
+      const size_t a = dense2_layout(FMT_FP8, Mc, N, K, 16).total;
       const size_t b = act_quant_ws(M, K);
       return a > b ? a : b;
     }
     case QL_OP_MXFP4: {
-      const size_t a = dense_layout(FMT_MXFP4, Mc, N, K).total;
+      size_t a = dense_layout(FMT_MXFP4, Mc, N, K).total;
+      const size_t a2 = dense2_layout(FMT_MXFP4, Mc, N, K, 128).total;
+      if (a2 > a) a = a2;
       const size_t b = act_quant_ws(M, K);
       return a > b ? a : b;
     }
@@ -203,43 +284,25 @@ ql_status qlinear_int8_w8a8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
   if (!al16(workspace)) return QL_ERR_ALIGNMENT;
   cudaStream_t st = (cudaStream_t)stream;
 
-  const int64_t Mc0 = M < 16 ? M : 16;
-  const DenseLayout lay = dense_layout(FMT_INT8, Mc0, N, K);
-  Carver c;
-  c.off = lay.total;
-  const size_t off_xq = c.take((size_t)M * K), off_xs = c.take((size_t)M * 4);
-  int8_t* xq = at<int8_t>(workspace, off_xq);
-  float* xs = at<float>(workspace, off_xs);
-  cudaError_t e = launch_quant_int8(x, (int)M, (int)K, ldx, xq, xs, xq_out, xs_out, st);
-  if (e != cudaSuccess) return cuda_status(e);
-
-  for (int64_t m0 = 0; m0 < M; m0 += 16) {
-    const int64_t Mc = (M - m0) < 16 ? (M - m0) : 16;
-    const SkinnyPlan p = skinny_plan(FMT_INT8, Mc, N, K);
-    const DenseLayout l = dense_layout(FMT_INT8, Mc, N, K);
-    SkinnyArgs a = {};
-    a.w = reinterpret_cast<const uint8_t*>(w);
-    a.ldw = ldw;
-    a.w_scale = w_scale;
-    a.w_scale_len = (int)w_scale_len;
-    a.x = xq + m0 * K;
-    a.ldx = K;
-    a.x_s = xs + m0;
-    a.M = (int)Mc;
-    a.N = (int)N;
-    a.K = (int)K;
-    a.y = y + m0 * ldy;
-    a.ldy = ldy;
-    a.bias = bias;
-    a.acc_out = acc_out ? acc_out + m0 * N : nullptr;
-    a.ks = p.sk.ks;
-    a.kc = p.sk.kc;
-    a.part = at<void>(workspace, l.part);
-    a.counters = at<unsigned>(workspace, l.counters);
-    a.pdl = 1;
-    e = launch_skinny(FMT_INT8, p.mt, EPI_INT8, a, dim3((unsigned)p.nb, (unsigned)p.sk.ks, 1), st, true);
-    if (e != cudaSuccess) return cuda_status(e);
-  }
+  Dense2Call d = {};
+  d.fmt = FMT_INT8;
+  d.x = x;
+  d.M = M;
+  d.K = K;
+  d.ldx = ldx;
+  d.w = reinterpret_cast<const uint8_t*>(w);
+  d.N = N;
+  d.ldw = ldw;
+  d.w_scale = w_scale;
+  d.w_scale_len = w_scale_len;
+  d.bias = bias;
+  d.y = y;
+  d.ldy = ldy;
+  d.acc_out = acc_out;
+  d.xq_out = xq_out;
+  d.xs_out = xs_out;
+  const ql_status s = run_dense2(d, workspace, st);
+  if (s != QL_OK) return s;
   if (path_out) *path_out = QL_PATH_INT8_SKINNY;
   return QL_OK;
 }
@@ -296,8 +359,23 @@ ql_status qlinear_fp8_block(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
   cudaStream_t st = (cudaStream_t)stream;
   if (!tc_path(act_mode)) {
     if (block_n % 16 != 0 || block_k % 64 != 0) return QL_ERR_UNSUPPORTED;
-    const ql_status s = run_skinny_bf16(FMT_FP8, x, M, K, ldx, w, N, ldw, w_scale, cdiv(K, block_k), block_n,
-                                        block_k, bias, y, ldy, workspace, st);
+    Dense2Call d = {};
+    d.fmt = FMT_FP8;
+    d.x = x;
+    d.M = M;
+    d.K = K;
+    d.ldx = ldx;
+    d.w = w;
+    d.N = N;
+    d.ldw = ldw;
+    d.wsb = w_scale;
+    d.lds = cdiv(K, block_k);
+    d.block_n = block_n;
+    d.block_k = block_k;
+    d.bias = bias;
+    d.y = y;
+    d.ldy = ldy;
+    const ql_status s = run_dense2(d, workspace, st);
     if (s == QL_OK && path_out) *path_out = QL_PATH_FP8_SKINNY;
     return s;
   }
@@ -344,8 +422,26 @@ ql_status qlinear_mxfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, co
   cudaStream_t st = (cudaStream_t)stream;
   if (!tc_path(act_mode)) {
     if (lds % 4 != 0 || (reinterpret_cast<uintptr_t>(w_scale) & 3) != 0) return QL_ERR_ALIGNMENT;
-    const ql_status s = run_skinny_bf16(FMT_MXFP4, x, M, K, ldx, w, N, ldw_bytes, w_scale, lds, 0, 0, bias, y, ldy,
-                                        workspace, st);
+    ql_status s;
+    if (mxfp4_v2_ok(K, lds, w_scale)) {
+      Dense2Call d = {};
+      d.fmt = FMT_MXFP4;
+      d.x = x;
+      d.M = M;
+      d.K = K;
+      d.ldx = ldx;
+      d.w = w;
+      d.N = N;
+      d.ldw = ldw_bytes;
+      d.wsb = w_scale;
+      d.lds = lds;
+      d.bias = bias;
+      d.y = y;
+      d.ldy = ldy;
+      s = run_dense2(d, workspace, st);
+    } else {
+      s = run_skinny_bf16(FMT_MXFP4, x, M, K, ldx, w, N, ldw_bytes, w_scale, lds, 0, 0, bias, y, ldy, workspace, st);
+    }
     if (s == QL_OK && path_out) *path_out = QL_PATH_MXFP4_SKINNY;
     return s;
   }
