@@ -17,10 +17,12 @@ inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Workspace layout: [0, 256) status word; [256, 256 + 4*kMaxTickets) split-K tickets, at the
-// same place for every op and shape, so that no call's data region ever overlaps the tickets
-// (the kernels return every ticket to zero); op regions follow, carved in order.
+// Workspace layout: [0, 256) status word (offset 0) and the skinny GEMM's activation hand-off
+// counters (offsets 32 and 36); [256, 256 + 4*kMaxTickets) split-K tickets, at the same place
+// for every op and shape, so that no call's data region ever overlaps them (the kernels return
+// every counter and ticket to zero); op regions follow, carved in order.
 constexpr size_t kMaxTickets = 65536;
+constexpr size_t kReadyOff = 32, kDoneOff = 36;
 constexpr size_t kTicketOff = 256;
 constexpr size_t kRegionsOff = kTicketOff + 4 * kMaxTickets;
 
@@ -84,7 +86,7 @@ Dense2Layout dense2_layout(int fmt, int64_t Mc, int64_t N, int64_t K, int block_
   Dense2Layout l;
   l.p = skinny2_plan(fmt, Mc, N, K, block_n);
   Carver c;
-  l.x16 = c.take((size_t)kXCopies * l.p.mp * K * 2);
+  l.x16 = c.take((size_t)kXCopies * Mc * l.p.kpad * 2);
   l.sc = c.take(16 * 4);
   l.part = c.take((size_t)l.p.nb * l.p.maxseg * 16 * S2_ROWS * 4);
   l.total = c.off;
@@ -170,27 +172,24 @@ ql_status run_dense2(const Dense2Call& d, void* workspace, cudaStream_t st) {
   for (int64_t m0 = 0; m0 < d.M; m0 += 16) {
     const int64_t Mc = (d.M - m0) < 16 ? (d.M - m0) : 16;
     const Dense2Layout l = dense2_layout(d.fmt, Mc, d.N, d.K, d.block_n);
-    uint16_t* x16 = at<uint16_t>(workspace, l.x16);
-    float* sc = at<float>(workspace, l.sc);
-    cudaError_t e;
-    if (d.fmt == FMT_INT8)
-      e = launch_prologue_int8(d.x + m0 * d.ldx, (int)Mc, l.p.mp, (int)d.K, d.ldx, x16, sc,
-                               d.xq_out ? d.xq_out + m0 * d.K : nullptr, d.xs_out ? d.xs_out + m0 : nullptr, st);
-    else
-      e = launch_prologue_bf16(d.x + m0 * d.ldx, (int)Mc, l.p.mp, (int)d.K, d.ldx, x16, sc, st);
-    if (e != cudaSuccess) return cuda_status(e);
     Skinny2Args a = {};
     a.M = (int)Mc;
     a.N = (int)d.N;
     a.K = (int)d.K;
+    a.x = d.x + m0 * d.ldx;
+    a.ldx = d.ldx;
+    a.x16 = at<uint16_t>(workspace, l.x16);
+    a.tokf = at<float>(workspace, l.sc);
+    a.xq_dbg = d.xq_out ? d.xq_out + m0 * d.K : nullptr;
+    a.xs_dbg = d.xs_out ? d.xs_out + m0 : nullptr;
+    a.ready = at<unsigned>(workspace, kReadyOff);
+    a.done = at<unsigned>(workspace, kDoneOff);
     a.wsb = d.wsb;
     a.lds = d.lds;
     a.block_n = d.block_n;
     a.block_k = d.block_k;
     a.w_scale = d.w_scale;
     a.w_scale_len = (int)d.w_scale_len;
-    a.x_s = sc;
-    a.tokscale = sc;
     a.y = d.y + m0 * d.ldy;
     a.ldy = d.ldy;
     a.bias = d.bias;
@@ -199,7 +198,7 @@ ql_status run_dense2(const Dense2Call& d, void* workspace, cudaStream_t st) {
     a.tickets = at<unsigned>(workspace, kTicketOff);
     a.status = at<uint32_t>(workspace, 0);
     a.wait_limit = g_wait_limit;
-    e = launch_skinny2(d.fmt, l.p, a, d.w, d.ldw, x16, st);
+    const cudaError_t e = launch_skinny2(d.fmt, l.p, a, d.w, d.ldw, st);
     if (e != cudaSuccess) return cuda_status(e);
   }
   return QL_OK;
@@ -233,7 +232,9 @@ size_t ql_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int to
       return dense2_layout(FMT_INT8, Mc, N, K, 128).total;
     case QL_OP_FP8_BLOCK: {
       // block_n is not known here: 16 (the smallest accepted) bounds the scale staging
-      const size_t a = dense2_layout(FMT_FP8, Mc, N, K, 16).total;
+      size_t a = dense2_layout(FMT_FP8, Mc, N, K, 16).total;
+      const size_t a1 = dense_layout(FMT_FP8, Mc, N, K).total;  // block_k not a power of two
+      if (a1 > a) a = a1;
       const size_t b = act_quant_ws(M, K);
       return a > b ? a : b;
     }
@@ -359,6 +360,14 @@ ql_status qlinear_fp8_block(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
   cudaStream_t st = (cudaStream_t)stream;
   if (!tc_path(act_mode)) {
     if (block_n % 16 != 0 || block_k % 64 != 0) return QL_ERR_UNSUPPORTED;
+    if ((block_k & (block_k - 1)) != 0) {
+      // the persistent kernel indexes block scales by shift: other block sizes stream through
+      // the register kernel
+      const ql_status s2 = run_skinny_bf16(FMT_FP8, x, M, K, ldx, w, N, ldw, w_scale, cdiv(K, block_k), block_n,
+                                           block_k, bias, y, ldy, workspace, st);
+      if (s2 == QL_OK && path_out) *path_out = QL_PATH_FP8_SKINNY;
+      return s2;
+    }
     Dense2Call d = {};
     d.fmt = FMT_FP8;
     d.x = x;

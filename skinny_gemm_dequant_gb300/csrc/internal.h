@@ -37,12 +37,13 @@ cudaError_t launch_moe_route(const MoeRouteArgs& r, cudaStream_t st);
 cudaError_t launch_moe_combine(const float* o, const int32_t* ids, const float* w, int M, int topk, int H,
                                uint16_t* y, cudaStream_t st);
 
-// persistent TMA-fed skinny GEMM (skinny2.cuh); the activation image is written kXCopies times
+// persistent TMA-fed skinny GEMM (skinny2.cuh); its activation image is written kXCopies times
 constexpr int kXCopies = 8;
 struct Skinny2Plan {
   int mt, mp;             // token tiles of 8, padded token rows
   int64_t nb;             // 128-row blocks
   int nk;                 // units per row block
+  int64_t kpad;           // K rounded up to whole units (row length of the activation image)
   int64_t total;          // nb * nk
   int grid;               // CTAs (one per SM)
   int maxseg;             // partial slots per row block
@@ -50,13 +51,9 @@ struct Skinny2Plan {
   size_t fp8_scale_bytes; // shared memory for the FP8 block-scale rows
 };
 Skinny2Plan skinny2_plan(int fmt, int64_t M, int64_t N, int64_t K, int block_n);
-cudaError_t launch_prologue_int8(const uint16_t* x, int M, int Mp, int K, int64_t ldx, uint16_t* x16, float* xs,
-                                 int8_t* xq_dbg, float* xs_dbg, cudaStream_t st);
-cudaError_t launch_prologue_bf16(const uint16_t* x, int M, int Mp, int K, int64_t ldx, uint16_t* x16, float* tokscale,
-                                 cudaStream_t st);
 struct Skinny2Args;
 cudaError_t launch_skinny2(int fmt, const Skinny2Plan& p, const Skinny2Args& a, const uint8_t* w, int64_t ldw,
-                           const uint16_t* x16, cudaStream_t st);
+                           cudaStream_t st);
 
 // split-K choice of the skinny kernel (shared by the workspace query and the launch)
 struct SplitK {
@@ -79,6 +76,8 @@ cudaError_t raise_smem_limit(F* kfn) {
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kfn);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+  // prefer the largest shared-memory carveout, so kernels sized for several CTAs per SM get them
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   return e;
 }
 

@@ -1,6 +1,6 @@
 // Persistent, TMA-fed skinny GEMM (M <= 16 tokens) for INT8, FP8-block and MXFP4 weights.
 //
-// Work: the weight matrix is cut into units of (128-row block, 128 weight bytes of K).  The
+// Work: the weight matrix is cut into units of (128-row block, 256 weight bytes of K).  The
 // units, ordered row block by row block, are split into one contiguous range per CTA, one CTA
 // per SM, so every SM streams the same number of weight bytes (no wave tail).  A row block split
 // between CTAs cf..cl is settled by cf, the CTA holding its first unit: those units are the last
@@ -8,45 +8,63 @@
 // themselves in (release); cf waits for the count (bounded), adds the partials in CTA order to
 // its own and writes the outputs, so results do not depend on timing.
 //
-// Inside a CTA, warp 16 is the producer: it keeps a ring of up to a dozen stages in flight, each
-// a 128x128-byte weight tile and the matching activation tile (f16, prepared once per call by
-// the prologue kernel), both loaded by TMA with 128-byte swizzling, plus (MXFP4) the tile's
-// per-32 scale bytes by cp.async.  Warps 0..7 consume, as 2 row groups (64 rows, four 16-row
-// MMA tiles) x 4 K quarters (two 16-byte chunks of every unit): a warp loads its activation
-// fragments once per unit and uses them for all four of its row tiles, which keeps the
-// shared-memory traffic per weight byte low.  ldmatrix gives each thread 4 weight bytes of a
-// chunk for rows g and g+8, converted to f16 in registers and fed to the warp MMA m16n8k16
-// (f32 accumulate) against the activations.  Each MMA draws all its K values from one 16-byte
-// chunk, i.e. from one 32-element MXFP4 scale group, so scales fold exactly per chunk (per
-// 32 K within a 128x128 FP8 block, exact integers for INT8).  The four K quarters of a row
-// group add their sums through shared memory when a row block ends.
+// Activations: the per-token preparation (INT8 quantisation, or the f16 image of bf16 values)
+// is part of this kernel, so a call is one launch.  After the grid-dependency wait, the
+// consumer warps of CTAs 0..M*copies-1 each write one (token, copy) row of an f16 image in
+// global memory, zero-padded to whole units, and count it in on a release counter; every
+// producer acquires the full count (bounded wait) before its first activation load.  The
+// weight stream does not wait: producers start loading weights as soon as the CTA starts,
+// which, with programmatic dependent launch, overlaps the previous kernel's last CTAs.  The
+// image is kept in several copies (CTA c reads copy c % copies) to spread the L2 traffic.
+//
+// Inside a CTA, warp 8 is the producer.  It keeps a ring of stages in flight; a stage holds one
+// unit and is filled by two TMA operations: the weights as one 3D box (128 rows x two 128-byte
+// K chunks, 32 KB) and the matching activations as one 4D box, plus (MXFP4) the unit's per-32
+// scale bytes by cp.async.  The TMA unit streams HBM at close to its peak only with large
+// operations: a 16 KB box per operation, or extra small boxes beside it, leave it well short.
+// A unit holding the ragged end of a row (K bytes not a multiple of 128) is loaded a chunk at
+// a time as 2D boxes, whose out-of-range bytes the TMA unit fills with zeros.
+//
+// Warps 0..7 consume, each a 16-row tile of the unit over its two chunks: ldmatrix gives each
+// thread 4 weight bytes of every 16-byte piece for rows g and g+8, converted to f16 in
+// registers and fed to the warp MMA m16n8k16 (f32 accumulate) against the activations.  Each
+// MMA draws all its K values from one 16-byte piece, i.e. from one 32-element MXFP4 scale
+// group, so scales fold exactly per piece (per 64 K inside one FP8 block; exact integers for
+// INT8).
 #pragma once
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
 namespace ql {
 
-constexpr int S2_TILES = 8;                      // 16-row tiles per unit
-constexpr int S2_RG = 2;                         // row groups of 4 tiles (64 rows)
-constexpr int S2_KQ = 4;                         // K quarters of a unit (2 chunks each)
-constexpr int S2_TPW = S2_TILES / S2_RG;         // tiles per consumer warp
-constexpr int S2_CONSUMERS = S2_RG * S2_KQ;      // 8 consumer warps
+constexpr int S2_CONSUMERS = 8;             // consumer warps, one 16-row tile each
 constexpr int S2_THREADS = 32 * (S2_CONSUMERS + 1);
-constexpr int S2_ROWS = 16 * S2_TILES;           // 128 weight rows per unit
-constexpr int S2_WB = 128;                       // weight bytes per row per unit
+constexpr int S2_ROWS = 16 * S2_CONSUMERS;  // 128 weight rows per unit
+constexpr int S2_CHUNKS = 2;                // 128-byte K chunks per unit
+constexpr int S2_WB = 128 * S2_CHUNKS;      // weight bytes per row per unit
 
 struct Skinny2Args {
   int M, N, K;
+  int wbytes;      // weight bytes of one row that hold K (K, or K/2 for MXFP4)
   int nk;          // units per row block
   int64_t total;   // row blocks x nk
   int maxseg;      // partial slots per row block
   const uint8_t* wsb;  // FP8: UE8M0 grid [ceil(N/bn), lds]; MXFP4: UE8M0 [N, lds]
   int64_t lds;
   int block_n, block_k;
+  int bk_shift;          // log2(block_k) (FP8: block_k is a power of two)
   const float* w_scale;  // INT8 per-channel / per-tensor scales
   int w_scale_len;
-  const float* x_s;       // INT8 per-token scales
-  const float* tokscale;  // bf16 activations: per-token 2^p undone in the epilogue
+  // activations and their preparation (done inside this kernel, see s2_prepare)
+  const uint16_t* x;      // bf16 [M, ldx]
+  int64_t ldx;
+  uint16_t* x16;          // f16 image [xcopies][M][kpad] (codes for INT8, x * 2^-p otherwise)
+  int64_t kpad;           // K rounded up to whole units
+  float* tokf;            // per token: INT8 x_s, bf16 paths 2^p (undone in the epilogue)
+  int8_t* xq_dbg;         // optional INT8 codes [M, K]
+  float* xs_dbg;          // optional INT8 x_s [M]
+  unsigned* ready;        // image rows written so far (release); back to 0 at kernel end
+  unsigned* done;         // producers past the hand-off; the last one resets both counters
   uint16_t* y;
   int64_t ldy;
   const uint16_t* bias;
@@ -61,21 +79,18 @@ struct Skinny2Args {
 
 template <int FMT>
 struct S2Traits {
-  static constexpr int KPU = (FMT == FMT_MXFP4) ? 256 : 128;  // K elements per unit
-  static constexpr int NXB = KPU / 64;                         // 64-element activation boxes per unit
-  static constexpr int SCB = (FMT == FMT_MXFP4) ? S2_ROWS * 8 : 0;  // scale bytes per unit
+  static constexpr int KPC = (FMT == FMT_MXFP4) ? 256 : 128;  // K elements per 128-byte chunk
+  static constexpr int KPU = KPC * S2_CHUNKS;                  // K elements per unit
+  static constexpr int NXB = KPU / 64;                         // 64-element activation slabs per unit
+  static constexpr int SCB = (FMT == FMT_MXFP4) ? S2_ROWS * 8 * S2_CHUNKS : 0;  // scale bytes per unit
 };
+
+// resident CTAs per SM: more warps per scheduler hide the consumers' dependency chains
+__host__ __device__ constexpr int s2_ctas_per_sm(int mt) { return mt == 1 ? 1 : 1; }
 
 template <int FMT, int MT>
 __host__ __device__ constexpr uint32_t s2_stage_bytes() {
   return S2_ROWS * S2_WB + S2Traits<FMT>::NXB * (8 * MT) * 128 + S2Traits<FMT>::SCB;
-}
-
-// shared memory for the K-quarter exchange at row-block ends:
-// [row group][3 non-lead quarters][4 tiles][32 lanes][4*MT] floats
-template <int MT>
-__host__ __device__ constexpr uint32_t s2_xchg_bytes() {
-  return S2_RG * (S2_KQ - 1) * S2_TPW * 32 * 4 * MT * 4;
 }
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -88,14 +103,35 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+// 8-byte copy global -> shared; src_bytes 0 writes zeros and reads nothing
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(tc::smem_u32(bar))
+      : "memory");
+}
 // named barrier of the consumer warps (the producer warp never joins it)
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// K slices per token of the activation image.  Every job reads its token's whole row (for the
+// amax): eight readers per row keep the L2 traffic on those lines low while splitting the
+// conversion eight ways; fewer when the grid is small.
+__host__ __device__ __forceinline__ int s2_slices(int M, int G) {
+  const int n = G / M;
+  return n < 1 ? 1 : (n > 8 ? 8 : n);
+}
 
 // CTA owning unit s when `total` units are split into G contiguous ranges [c*T/G, (c+1)*T/G)
 __device__ __forceinline__ int s2_cta_of(int64_t s, int64_t T, int G) {
@@ -107,14 +143,141 @@ __device__ __forceinline__ uint32_t sw128(int row, int byte) {
   return (uint32_t)(row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15)));
 }
 
+__device__ __forceinline__ float bf16x2_absmax(uint32_t w) {
+  return fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xFFFF0000u)));
+}
+
+// INT8 code of x for the per-token scale s (> 0, normal) with r = RN(1/s): rint(RN(x/s))
+// clamped to +-127, bit for bit.  The product y = RN(x*r) is within 127*1.2e-7 < 1.6e-5 of x/s
+// and RN(x/s) within 7.7e-6 of it, so rint(y) and rint(RN(x/s)) can only differ when y lies
+// within 2.4e-5 of a half-integer; there (rarely) the IEEE quotient is taken instead.
+__device__ __forceinline__ float s2_code(float xv, float s, float r) {
+  float y = xv * r;
+  if (fabsf((y - floorf(y)) - 0.5f) < 6.1e-5f) y = __fdiv_rn(xv, s);
+  return fminf(fmaxf(rintf(y), -127.f), 127.f);
+}
+
+// Activation image, one job = (token m, slice sl of nsl): the 256 consumer threads of a CTA
+// (thread tid) find the token's amax over all of K, then write their slice of the row into
+// every copy of the image.  INT8: dynamic per-token quantisation, x_s = amax/127 and codes
+// clamp(rint(x/x_s), -127, 127) with IEEE rounding, as exact f16 integers.  bf16 activations:
+// f16 image x * 2^-p with p from the token's amax (scaled amax in [2^14, 2^15)), so every bf16
+// value keeps its full significand unless it is below 2^-24 of the amax.  Slice 0 also writes
+// the per-token factor the epilogue applies (x_s or 2^p) and the INT8 x_s debug output.
+template <int FMT>
+__device__ void s2_prepare(const Skinny2Args& a, int m, int sl, int nsl, int tid, float* red) {
+  constexpr int V = 8;  // 16-byte vectors a thread holds: one pass over x for K <= 256*8*8
+  const uint16_t* xr = a.x + (int64_t)m * a.ldx;
+  const int nvec = a.K / 8;
+  const int v0 = (int)((int64_t)sl * nvec / nsl), v1 = (int)((int64_t)(sl + 1) * nvec / nsl);
+  const bool one_pass = nvec <= V * 256;
+  uint4 v[V];
+  float amax = 0.f;
+  if (one_pass) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const int i = tid + 256 * j;
+      v[j] = i < nvec ? *reinterpret_cast<const uint4*>(xr + 8 * i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < V; ++j)
+      amax = fmaxf(amax, fmaxf(fmaxf(bf16x2_absmax(v[j].x), bf16x2_absmax(v[j].y)),
+                               fmaxf(bf16x2_absmax(v[j].z), bf16x2_absmax(v[j].w))));
+  } else {
+    for (int i = tid; i < nvec; i += 256) {
+      const uint4 u = *reinterpret_cast<const uint4*>(xr + 8 * i);
+      amax = fmaxf(amax, fmaxf(fmaxf(bf16x2_absmax(u.x), bf16x2_absmax(u.y)), fmaxf(bf16x2_absmax(u.z), bf16x2_absmax(u.w))));
+    }
+  }
+  amax = warp_max(amax);
+  if ((tid & 31) == 0) red[tid >> 5] = amax;
+  consumer_sync();
+  amax = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])), fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7])));
+  float f, inv = 1.f;  // INT8: f = x_s and inv = RN(1/x_s); else f = 2^p and inv = 2^-p
+  bool fast = true;    // INT8: x_s normal, so the reciprocal path is exact (see s2_code)
+  if constexpr (FMT == FMT_INT8) {
+    f = __fdiv_rn(amax, 127.0f);
+    fast = f >= 1.17549435e-38f;
+    if (fast) inv = __frcp_rn(f);
+  } else {
+    int p = 0;
+    if (amax > 0.f) p = max((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127, -126) - 14;
+    p = max(-100, min(100, p));
+    f = __uint_as_float((uint32_t)(127 + p) << 23);
+    inv = __uint_as_float((uint32_t)(127 - p) << 23);
+  }
+  const int64_t cstride = (int64_t)a.M * a.kpad;  // elements between copies
+  uint16_t* out = a.x16 + (int64_t)m * a.kpad;
+  auto conv = [&](const uint4 u, int i) {
+    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+    uint32_t h[4];
+    if constexpr (FMT == FMT_INT8) {
+      float qv[8];
+      uint32_t qb[2] = {0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float xv = (e & 1) ? __uint_as_float(wv[e >> 1] & 0xFFFF0000u) : __uint_as_float(wv[e >> 1] << 16);
+        float q = 0.f;
+        if (fast)
+          q = s2_code(xv, f, inv);
+        else if (f > 0.f)
+          q = fminf(fmaxf(rintf(__fdiv_rn(xv, f)), -127.f), 127.f);
+        qv[e] = q;
+        qb[e >> 2] |= ((uint32_t)((int)q & 0xFF)) << (8 * (e & 3));
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) h[j] = pack_f16x2(qv[2 * j], qv[2 * j + 1]);  // exact: |q| <= 127
+      if (a.xq_dbg) *reinterpret_cast<uint2*>(a.xq_dbg + (int64_t)m * a.K + 8 * i) = make_uint2(qb[0], qb[1]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        h[j] = pack_f16x2(__uint_as_float(wv[j] << 16) * inv, __uint_as_float(wv[j] & 0xFFFF0000u) * inv);
+    }
+    const uint4 hv = make_uint4(h[0], h[1], h[2], h[3]);
+    for (int cp = 0; cp < a.xcopies; ++cp) *reinterpret_cast<uint4*>(out + cp * cstride + 8 * i) = hv;
+  };
+  if (one_pass) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const int i = tid + 256 * j;
+      if (i >= v0 && i < v1) conv(v[j], i);
+    }
+  } else {
+    for (int i = v0 + tid; i < v1; i += 256) conv(*reinterpret_cast<const uint4*>(xr + 8 * i), i);
+  }
+  if (sl == nsl - 1)  // the tail past K (to whole units) is zero
+    for (int i = nvec + tid; i < (int)(a.kpad / 8); i += 256)
+      for (int cp = 0; cp < a.xcopies; ++cp) *reinterpret_cast<uint4*>(out + cp * cstride + 8 * i) = make_uint4(0, 0, 0, 0);
+  if (sl == 0 && tid == 0) {
+    a.tokf[m] = f;
+    if (FMT == FMT_INT8 && a.xs_dbg) a.xs_dbg[m] = f;
+  }
+  consumer_sync();  // red[] is reused by the next job
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, int x, int y, int z, int w,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(tc::smem_u32(bar))
+      : "memory");
+}
+
+// tmW: 3D view {128 bytes, N rows, full 128-byte chunks} (strides ldw, 128), box {128, 128, 2}
+// tmW2: 2D view {wbytes, N}, box {128, 128}: units holding a partial chunk
+// tmX: 4D view of the activation image {64 f16, M rows, copies, kpad/64}, box {64, Mp, 1, NXB}
+//      (rows M..Mp-1 of the box are out of range and read as zeros)
 template <int FMT, int MT>
-__global__ void __launch_bounds__(S2_THREADS, 1)
-    skinny2_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const __grid_constant__ Skinny2Args a) {
+__global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
+    skinny2_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
+                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Skinny2Args a) {
   using Tr = S2Traits<FMT>;
   constexpr int Mp = 8 * MT;
-  constexpr uint32_t W_BYTES = S2_ROWS * S2_WB;
-  constexpr uint32_t X_BOX = Mp * 128;
+  constexpr uint32_t W_CHUNK = S2_ROWS * 128;  // one 128-byte chunk of all 128 rows (16 KB)
+  constexpr uint32_t W_BYTES = W_CHUNK * S2_CHUNKS;
+  constexpr uint32_t X_BOX = Mp * 128;         // one 64-element slab of all token rows
+  constexpr uint32_t X_BYTES = Tr::NXB * X_BOX;
   constexpr uint32_t STAGE = s2_stage_bytes<FMT, MT>();
   constexpr bool kInt = (FMT == FMT_INT8);
   extern __shared__ uint8_t smem_raw[];
@@ -122,10 +285,13 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
   const int S = a.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * STAGE);
   uint64_t* empty = full + S;
-  float* xchg = reinterpret_cast<float*>(empty + S);                        // pair exchange
-  uint8_t* fp8sc = reinterpret_cast<uint8_t*>(xchg) + s2_xchg_bytes<MT>();  // FP8 scale rows
+  uint8_t* fp8sc = reinterpret_cast<uint8_t*>(empty + S);  // FP8 scale rows of this CTA's row blocks
   __shared__ int s_abort;
 
+  // the next kernel in the stream (the next call's prologue) may launch now: it waits for this
+  // grid to finish before it touches memory, and meanwhile the GEMM after it can take each SM
+  // this grid leaves and start streaming its own weights
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, c = blockIdx.x;
   const int64_t T = a.total;
@@ -140,7 +306,6 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
 
   // FP8 block scales: the rows of every n-block this CTA's units touch, copied up front
   const int rb_first = (int)(s0 / nk);
-  const int nbr = (a.block_n > 0) ? (S2_ROWS / a.block_n + 2) : 0;  // n-blocks a 128-row block spans
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       tc::mbar_init(&full[i], FMT == FMT_MXFP4 ? 1 + 32 : 1);
@@ -152,179 +317,220 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
     tc::tma_prefetch_desc(&tmX);
   }
   if constexpr (FMT == FMT_FP8) {
-    const int rb_last = (s1 > s0) ? (int)((s1 - 1) / nk) : rb_first;
+    const int nbr = S2_ROWS / a.block_n + 2;  // n-blocks a 128-row block can touch
+    const int rb_last = (int)((s1 - 1) / nk);
     const int nrow_blocks = rb_last - rb_first + 1;
     const int nb0 = (rb_first * S2_ROWS) / a.block_n;
     const int nb_count = min(nrow_blocks * nbr, (int)((a.N + a.block_n - 1) / a.block_n) - nb0);
-    for (int i = threadIdx.x; i < nb_count * a.lds; i += blockDim.x)
-      fp8sc[i] = a.wsb[(int64_t)nb0 * a.lds + i];
+    for (int i = threadIdx.x; i < nb_count * a.lds; i += blockDim.x) fp8sc[i] = a.wsb[(int64_t)nb0 * a.lds + i];
   }
   __syncthreads();
 
   if (warp == S2_CONSUMERS) {
     // ------------------------------------------------------------ producer warp
     const int pre = (int)((int64_t)S < s1 - s0 ? (int64_t)S : s1 - s0);
-    const int xrow = (c % a.xcopies) * Mp;  // first row of this CTA's copy of the activations
+    const int xcp = c % a.xcopies;  // this CTA's copy of the activation image
+    const bool whole_chunks = (a.wbytes & 127) == 0;
+    const int ksc = a.K / 32;  // MXFP4 scale bytes of a row that belong to K
     bool ok = true;
-    int64_t issued = s0;
-    for (int64_t s = s0; s < s1; ++s) {
-      const int i = (int)(s - s0);
-      const int slot = i % S;
+    const int n_units = (int)(s1 - s0);
+    int issued = 0;
+    // unit counters kept incrementally: no divisions in the loop
+    int rb = rb_first, kt = (int)(s0 - (int64_t)rb_first * nk);
+    int slot = 0;
+    uint32_t phase = 0;  // (i / S) & 1
+    for (int i = 0; i < n_units; ++i) {
       int got = 1;
-      if (lane == 0 && i >= S) got = tc::mbar_wait(&empty[slot], ((uint32_t)(i / S) - 1) & 1, lim, abort);
+      if (lane == 0 && i >= S) got = tc::mbar_wait(&empty[slot], phase ^ 1u, lim, abort);
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) {
         if (lane == 0) fail();
         ok = false;
         break;
       }
-      const int rb = (int)(s / nk), kt = (int)(s % nk);
-      uint8_t* st = smem + (size_t)slot * STAGE;
+      const uint32_t st = tc::smem_u32(smem + (size_t)slot * STAGE);
       if (lane == 0) {
-        tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + Tr::NXB * X_BOX);
-        tc::tma_load_2d(st, &tmW, kt * S2_WB, rb * S2_ROWS, &full[slot]);
+        // weights: chunks 2kt, 2kt+1 of rows rb*128.. -> smem [chunk][row][128 B]
+        if (whole_chunks || (kt + 1) * S2_WB <= a.wbytes) {
+          tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + X_BYTES);
+          tma_load_3d(st, &tmW, 0, rb * S2_ROWS, kt * S2_CHUNKS, &full[slot]);
+        } else {
+          // the row ends inside this unit, off a chunk boundary: a chunk at a time from the 2D
+          // view, whose bytes past the end (a whole chunk, possibly) are filled with zeros
+          tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + X_BYTES);
+          tc::tma_load_2d(smem + (size_t)slot * STAGE, &tmW2, kt * S2_WB, rb * S2_ROWS, &full[slot]);
+          tc::tma_load_2d(smem + (size_t)slot * STAGE + W_CHUNK, &tmW2, kt * S2_WB + 128, rb * S2_ROWS, &full[slot]);
+        }
         if (i >= pre) {
-#pragma unroll
-          for (int b = 0; b < Tr::NXB; ++b)
-            tc::tma_load_2d(st + W_BYTES + b * X_BOX, &tmX, kt * Tr::KPU + b * 64, xrow, &full[slot]);
+          tma_load_4d(st + W_BYTES, &tmX, 0, 0, xcp, kt * Tr::NXB, &full[slot]);
         } else if (i == pre - 1) {
-          // activations come from the prologue kernel: wait for it once, then load the
-          // activation tiles of the stages already in flight
+          // the activation image is written by this grid's consumer warps: wait (bounded) until
+          // all its rows are in, then load the activation tiles of the stages already in flight.
+          // On a timeout the status is flagged and the loads still go out, so no stage waits
+          // forever.
+          // the counters belong to the previous call until its grid is done: wait for it first
           pdl_wait();
-          for (int j = 0; j < pre; ++j) {
-            const int64_t sj = s0 + j;
-            uint8_t* stj = smem + (size_t)(j % S) * STAGE;
-#pragma unroll
-            for (int b = 0; b < Tr::NXB; ++b)
-              tc::tma_load_2d(stj + W_BYTES + b * X_BOX, &tmX, (int)(sj % nk) * Tr::KPU + b * 64, xrow, &full[j % S]);
+          const unsigned need = (unsigned)(a.M * s2_slices(a.M, G));
+          for (uint32_t n = 0;; ++n) {
+            unsigned v;
+            asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(a.ready) : "memory");
+            if (v >= need) break;
+            if (n >= lim) {
+              fail();
+              break;
+            }
+            __nanosleep(32);
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // generic writes -> TMA reads
+          // the last producer past this point returns both counters to zero for the next call
+          if (atomicAdd(a.done, 1u) == (unsigned)G - 1) {
+            *a.ready = 0;
+            *a.done = 0;
+          }
+          int ktj = (int)(s0 - (int64_t)rb_first * nk);
+          for (int j = 0; j < pre; ++j) {  // pre <= S: stage j is slot j
+            const uint32_t stj = tc::smem_u32(smem + (size_t)j * STAGE);
+            tma_load_4d(stj + W_BYTES, &tmX, 0, 0, xcp, ktj * Tr::NXB, &full[j]);
+            if (++ktj == nk) ktj = 0;
           }
         }
       }
       if constexpr (FMT == FMT_MXFP4) {
-        // per-32 scale bytes of the unit: 128 rows x 8 bytes, 4 rows per lane
-        const uint32_t sc = tc::smem_u32(st + W_BYTES + Tr::NXB * X_BOX);
+        // per-32 scale bytes of the unit: 128 rows x (8 bytes per chunk); bytes past K read as 0
+        const uint32_t sc = st + W_BYTES + X_BYTES;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = lane * 4 + j;
+        for (int j = 0; j < 8; ++j) {
+          const int r = lane * 4 + (j >> 1), h = j & 1;
           const int n = min(rb * S2_ROWS + r, a.N - 1);
-          cp_async8(sc + r * 8, a.wsb + (int64_t)n * a.lds + kt * 8);
+          const int b0 = kt * 16 + h * 8;
+          cp_async8(sc + r * 16 + h * 8, a.wsb + (int64_t)n * a.lds + (b0 < ksc ? b0 : 0), b0 < ksc ? 8u : 0u);
         }
         cp_async_mbar_arrive(&full[slot]);
       }
-      issued = s + 1;
+      issued = i + 1;
+      if (++kt == nk) {
+        kt = 0;
+        ++rb;
+      }
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
+      }
     }
     if (!ok && lane == 0) {
       // no copy may land after the CTA exits: wait for every stage still in flight
-      for (int64_t s = max(s0, issued - S); s < issued; ++s) {
-        const int i = (int)(s - s0);
+      for (int i = max(0, issued - S); i < issued; ++i)
         tc::mbar_wait(&full[i % S], (uint32_t)(i / S) & 1, 1u << 22, nullptr);
-      }
     }
     if constexpr (FMT == FMT_MXFP4) asm volatile("cp.async.wait_all;" ::: "memory");
     return;
   }
 
   // -------------------------------------------------------------- consumer warps
+  // activations may come from the previous kernel in the stream: wait for it, then write this
+  // CTA's rows of the activation image (rows j = c, c + G, ... of M x copies) and count them in
   pdl_wait();
-  const int g = lane >> 2, t = lane & 3;
-  const int rg = warp / S2_KQ;   // row group: tiles 4*rg .. 4*rg+3 (rows 64*rg ..)
-  const int kq = warp % S2_KQ;   // K quarter of every unit: chunks 2*kq, 2*kq+1
-  const bool lead = kq == 0;     // the warp of the row group that writes results
-  // per-token epilogue factors of this thread's columns (x_s or 2^p), loaded once
-  float colf[MT][2];
-#pragma unroll
-  for (int m = 0; m < MT; ++m)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int col = 2 * t + e + 8 * m;
-      colf[m][e] = col < a.M ? (kInt ? a.x_s[col] : a.tokscale[col]) : 0.f;
+  {
+    __shared__ float s_red[S2_CONSUMERS];
+    const int nsl = s2_slices(a.M, G);
+    const int njobs = a.M * nsl;
+    unsigned mine = 0;
+    for (int j = c; j < njobs; j += G, ++mine) s2_prepare<FMT>(a, j % a.M, j / a.M, nsl, threadIdx.x, s_red);
+    if (mine) {
+      // the rows are read by TMA (async proxy) in other CTAs: proxy fence, then one release
+      // (cumulative over the CTA's writes, ordered before it by the barrier)
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      consumer_sync();
+      if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a.ready), "r"(mine) : "memory");
     }
-  // ldmatrix addressing: lane L feeds row (L & 7) + 8*((L >> 3) & 1) of its matrix, chunk L >> 4
-  const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int lchk = lane >> 4;
-  // accumulator element r of tile i, token tile m: row 16*(4*rg+i) + g + 8*(r>=2), col 2t+(r&1)+8m
-  float acc[S2_TPW][MT][4];
-  int32_t acci[S2_TPW][MT][4];
-  float own[S2_TPW][MT][4];  // partial sums of the block this CTA settles (lead warps)
+  }
+  const int g = lane >> 2, t = lane & 3;
+  const int w = warp;  // 16-row tile of the unit
+  // per-token epilogue factors of this thread's columns (x_s or 2^p), loaded at the first
+  // segment end: a stage has arrived by then, and its activations were loaded only after the
+  // image, factors included, was complete
+  float colf[MT][2] = {};
+  bool have_colf = false;
+  // ldmatrix addressing: lane L feeds row 16w + (L & 7) + 8*((L >> 3) & 1) of piece 2p + (L >> 4)
+  const int lrow = 16 * w + (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int lpc = lane >> 4;
+  float acc[MT][4];
+  int32_t acci[MT][4];
+  float own[MT][4];  // partial sums of the block this CTA settles
   int settle_rb = -1;
   bool ok = true;
-  int64_t s = s0;
-  while (s < s1) {
-    const int rb = (int)(s / nk);
-    const int kt0 = (int)(s % nk);
-    const int64_t seg_end = min(s1, (int64_t)(rb + 1) * nk);
+  int rb = rb_first;
+  int kt = (int)(s0 - (int64_t)rb_first * nk);
+  int slot = 0;
+  uint32_t phase = 0;
+  int left = (int)(s1 - s0);  // units still to consume
+  while (left > 0) {
+    const int kt0 = kt;
+    const int seg_units = min(nk - kt, left);  // this row block's units in the range
 #pragma unroll
-    for (int i = 0; i < S2_TPW; ++i)
+    for (int m = 0; m < MT; ++m)
 #pragma unroll
-      for (int m = 0; m < MT; ++m)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) { acc[i][m][r] = 0.f; acci[i][m][r] = 0; }
-    const int row_g = rb * S2_ROWS + 64 * rg;  // first row of this warp's row group
-    // FP8 scale row of each tile's n-block (block_n >= 16 may split a row group)
-    const uint8_t* sc_row[S2_TPW];
-#pragma unroll
-    for (int ti = 0; ti < S2_TPW; ++ti) sc_row[ti] = nullptr;
-    if constexpr (FMT == FMT_FP8) {
-#pragma unroll
-      for (int ti = 0; ti < S2_TPW; ++ti) {
-        const int nb = min(row_g + 16 * ti, a.N - 1) / a.block_n;
-        sc_row[ti] = fp8sc + (int64_t)(nb - (rb_first * S2_ROWS) / a.block_n) * a.lds;
+      for (int r = 0; r < 4; ++r) {
+        acc[m][r] = 0.f;
+        acci[m][r] = 0;
       }
+    const int row_w = rb * S2_ROWS + 16 * w;  // first row of this warp's tile
+    const uint8_t* sc_row = nullptr;          // FP8 scale row of this warp's n-block
+    if constexpr (FMT == FMT_FP8) {
+      const int nb = min(row_w, a.N - 1) / a.block_n;
+      sc_row = fp8sc + (int64_t)(nb - (rb_first * S2_ROWS) / a.block_n) * a.lds;
     }
-    for (; s < seg_end; ++s) {
-      const int i = (int)(s - s0);
-      const int slot = i % S;
+    for (int u = 0; u < seg_units; ++u, ++kt) {
       int got = 0;
-      if (lane == 0 && ok) got = tc::mbar_wait(&full[slot], (uint32_t)(i / S) & 1, lim, abort);
+      if (lane == 0 && ok) got = tc::mbar_wait(&full[slot], phase, lim, abort);
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) {
         // timed out (or another role did): stop computing but keep walking the units, so
         // every consumer warp still reaches the same named barriers below
         if (lane == 0 && ok) fail();
         ok = false;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1u;
+        }
         continue;
       }
-      const int kt = (int)(s % nk);
       const uint32_t st = tc::smem_u32(smem + (size_t)slot * STAGE);
       const uint32_t xt = st + W_BYTES;
-      // weight fragments of the warp's 4 tiles x 2 chunks: q[i][0..3] = (rows g, chunk c),
-      // (g+8, c), (g, c+1), (g+8, c+1) of tile i, c = 2*kq
-      uint32_t q[S2_TPW][4];
+      // INT8: the unit's sums in two fp32 chains; every partial sum is an integer of at most
+      // 256 x 127 x 127 < 2^24 in magnitude, so they are exact and convert once per unit
+      float ui[2][MT][4];
 #pragma unroll
-      for (int ti = 0; ti < S2_TPW; ++ti)
-        ldmatrix_x4(st + sw128(16 * (S2_TPW * rg + ti) + lrow, (2 * kq + lchk) * 16), q[ti][0], q[ti][1], q[ti][2],
-                    q[ti][3]);
-      if constexpr (FMT == FMT_MXFP4) {
-        // activation fragments of the two chunks (each 32 K = one scale group), both halves
-        uint2 xv[2][2][MT];
+      for (int e = 0; e < 2; ++e)
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int m = 0; m < MT; ++m) ui[e][m][0] = ui[e][m][1] = ui[e][m][2] = ui[e][m][3] = 0.f;
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+      for (int ck = 0; ck < S2_CHUNKS; ++ck) {
+        const uint32_t wt = st + ck * W_CHUNK;
+        // the chunk's 8 sixteen-byte pieces for this warp's 16 rows (4 ldmatrix.x4):
+        // q[p] = (row g, piece 2p), (g+8, 2p), (g, 2p+1), (g+8, 2p+1)
+        uint32_t q[4][4];
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-              const int kl = 32 * (2 * kq + j) + 8 * t + 4 * h;
-              xv[j][h][m] = lds64(xt + (kl >> 6) * X_BOX + sw128(g + 8 * m, (kl & 63) * 2));
-            }
-        // scale bytes 2*kq, 2*kq+1 of rows g and g+8 of each tile
-        const uint32_t sbase = st + W_BYTES + Tr::NXB * X_BOX;
-        uint32_t sa[S2_TPW], sb[S2_TPW];
+        for (int p = 0; p < 4; ++p)
+          ldmatrix_x4(wt + sw128(lrow, (2 * p + lpc) * 16), q[p][0], q[p][1], q[p][2], q[p][3]);
+        if constexpr (FMT == FMT_MXFP4) {
+          // scale bytes of rows g and g+8 for the chunk's 8 groups
+          const uint32_t sbase = st + W_BYTES + X_BYTES;
+          const uint2 sa8 = lds64(sbase + (16 * w + g) * 16 + ck * 8);
+          const uint2 sb8 = lds64(sbase + (16 * w + g + 8) * 16 + ck * 8);
 #pragma unroll
-        for (int ti = 0; ti < S2_TPW; ++ti) {
-          const int r0 = 16 * (S2_TPW * rg + ti) + g;
-          const uint2 va = lds64(sbase + r0 * 8), vb = lds64(sbase + (r0 + 8) * 8);
-          sa[ti] = (kq < 2 ? va.x : va.y) >> (16 * (kq & 1));
-          sb[ti] = (kq < 2 ? vb.x : vb.y) >> (16 * (kq & 1));
-        }
-        // chunk by chunk: MMAs of the 4 tiles, then the per-row scale fold of that chunk
+          for (int pc = 0; pc < 8; ++pc) {  // piece = one 32-element scale group
+            const uint32_t qa = q[pc >> 1][2 * (pc & 1)], qb = q[pc >> 1][2 * (pc & 1) + 1];
+            // this thread's 8 weights of the piece are K 8t..8t+7: the activations of those
+            // K are 16 contiguous bytes of the token's row
+            const int kx = 32 * pc + 8 * t;  // K within the chunk
+            uint4 xv[MT];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          float blk[S2_TPW][MT][4];
+            for (int m = 0; m < MT; ++m)
+              xv[m] = lds128(xt + (4 * ck + (kx >> 6)) * X_BOX + sw128(g + 8 * m, (kx & 63) * 2));
+            float blk[MT][4];
 #pragma unroll
-          for (int ti = 0; ti < S2_TPW; ++ti) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m) blk[ti][m][0] = blk[ti][m][1] = blk[ti][m][2] = blk[ti][m][3] = 0.f;
-            const uint32_t qa = q[ti][2 * j], qb = q[ti][2 * j + 1];
+            for (int m = 0; m < MT; ++m) blk[m][0] = blk[m][1] = blk[m][2] = blk[m][3] = 0.f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const uint32_t a0 = e2m1x2_to_f16x2(qa >> (16 * h));
@@ -332,182 +538,154 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
               const uint32_t a1 = e2m1x2_to_f16x2(qb >> (16 * h));
               const uint32_t a3 = e2m1x2_to_f16x2(qb >> (16 * h + 8));
 #pragma unroll
-              for (int m = 0; m < MT; ++m) mma_f16_16816(blk[ti][m], a0, a1, a2, a3, xv[j][h][m].x, xv[j][h][m].y);
+              for (int m = 0; m < MT; ++m)
+                mma_f16_16816(blk[m], a0, a1, a2, a3, h ? xv[m].z : xv[m].x, h ? xv[m].w : xv[m].y);
             }
-          }
-          if (j == 1) {  // every shared-memory fragment has been consumed: hand the stage back
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&empty[slot]);
-          }
-#pragma unroll
-          for (int ti = 0; ti < S2_TPW; ++ti) {
-            const float fa = ue8m0_to_f32(sa[ti] >> (8 * j)), fb = ue8m0_to_f32(sb[ti] >> (8 * j));
+            const float fa = ue8m0_to_f32((pc < 4 ? sa8.x : sa8.y) >> (8 * (pc & 3)));
+            const float fb = ue8m0_to_f32((pc < 4 ? sb8.x : sb8.y) >> (8 * (pc & 3)));
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-              acc[ti][m][0] = fmaf(blk[ti][m][0], fa, acc[ti][m][0]);
-              acc[ti][m][1] = fmaf(blk[ti][m][1], fa, acc[ti][m][1]);
-              acc[ti][m][2] = fmaf(blk[ti][m][2], fb, acc[ti][m][2]);
-              acc[ti][m][3] = fmaf(blk[ti][m][3], fb, acc[ti][m][3]);
+              acc[m][0] = fmaf(blk[m][0], fa, acc[m][0]);
+              acc[m][1] = fmaf(blk[m][1], fa, acc[m][1]);
+              acc[m][2] = fmaf(blk[m][2], fb, acc[m][2]);
+              acc[m][3] = fmaf(blk[m][3], fb, acc[m][3]);
             }
           }
-        }
-      } else {
-        uint2 xv[2][MT];
+        } else if constexpr (FMT == FMT_INT8) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-#pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            const int kl = 16 * (2 * kq + j) + 4 * t;
-            xv[j][m] = lds64(xt + (kl >> 6) * X_BOX + sw128(g + 8 * m, (kl & 63) * 2));
-          }
-        float blk[S2_TPW][MT][4];
-#pragma unroll
-        for (int ti = 0; ti < S2_TPW; ++ti) {
-#pragma unroll
-          for (int m = 0; m < MT; ++m) blk[ti][m][0] = blk[ti][m][1] = blk[ti][m][2] = blk[ti][m][3] = 0.f;
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const uint32_t qa = q[ti][2 * j], qb = q[ti][2 * j + 1];
+          for (int pc = 0; pc < 8; ++pc) {
+            const uint32_t qa = q[pc >> 1][2 * (pc & 1)], qb = q[pc >> 1][2 * (pc & 1) + 1];
             uint32_t a0, a1, a2, a3;
-            if constexpr (FMT == FMT_INT8) {
-              s8x4_to_f16x2x2(qa, a0, a2);
-              s8x4_to_f16x2x2(qb, a1, a3);
-            } else {
-              a0 = e4m3x2_to_f16x2((uint16_t)(qa & 0xFFFFu));
-              a2 = e4m3x2_to_f16x2((uint16_t)(qa >> 16));
-              a1 = e4m3x2_to_f16x2((uint16_t)(qb & 0xFFFFu));
-              a3 = e4m3x2_to_f16x2((uint16_t)(qb >> 16));
+            s8x4_to_f16x2x2(qa, a0, a2);
+            s8x4_to_f16x2x2(qb, a1, a3);
+            const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(g + 8 * m, (kx & 63) * 2));
+              mma_f16_16816(ui[pc & 1][m], a0, a1, a2, a3, xv.x, xv.y);
             }
-#pragma unroll
-            for (int m = 0; m < MT; ++m) mma_f16_16816(blk[ti][m], a0, a1, a2, a3, xv[j][m].x, xv[j][m].y);
           }
-        }
-        // every shared-memory fragment has been consumed: hand the stage back before folding
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&empty[slot]);
-        if constexpr (FMT == FMT_INT8) {
-          // each tile's chain sums 2 x 16 products of at most 127 x 127: exact in fp32
+        } else {
 #pragma unroll
-          for (int ti = 0; ti < S2_TPW; ++ti)
+          for (int hb = 0; hb < 2; ++hb) {  // 64-K halves of the chunk: the FP8 fold granularity
+            float blk[2][MT][4];            // two chains so consecutive MMAs are independent
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+              for (int m = 0; m < MT; ++m) blk[e][m][0] = blk[e][m][1] = blk[e][m][2] = blk[e][m][3] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int pc = 4 * hb + j;
+              const uint32_t qa = q[pc >> 1][2 * (pc & 1)], qb = q[pc >> 1][2 * (pc & 1) + 1];
+              const uint32_t a0 = e4m3x2_to_f16x2((uint16_t)(qa & 0xFFFFu));
+              const uint32_t a2 = e4m3x2_to_f16x2((uint16_t)(qa >> 16));
+              const uint32_t a1 = e4m3x2_to_f16x2((uint16_t)(qb & 0xFFFFu));
+              const uint32_t a3 = e4m3x2_to_f16x2((uint16_t)(qb >> 16));
+              const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
+#pragma unroll
+              for (int m = 0; m < MT; ++m) {
+                const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(g + 8 * m, (kx & 63) * 2));
+                mma_f16_16816(blk[j & 1][m], a0, a1, a2, a3, xv.x, xv.y);
+              }
+            }
+            const int k0 = (kt * S2_CHUNKS + ck) * 128 + 64 * hb;  // first K of this half
+            // block_k is a power of two; K past the last block (zero weights) has no scale byte
+            const float f = k0 < a.K ? ue8m0_to_f32(sc_row[min(k0, a.K - 1) >> a.bk_shift]) : 0.f;
 #pragma unroll
             for (int m = 0; m < MT; ++m)
 #pragma unroll
-              for (int r = 0; r < 4; ++r) acci[ti][m][r] += __float2int_rn(blk[ti][m][r]);
-        } else if (kt * 128 + 32 * kq < a.K) {  // a K tail past the last block has no scale
-          const int kb = (kt * 128 + 32 * kq) / a.block_k;
-#pragma unroll
-          for (int ti = 0; ti < S2_TPW; ++ti) {
-            const float f = ue8m0_to_f32(sc_row[ti][kb]);
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
-              for (int r = 0; r < 4; ++r) acc[ti][m][r] = fmaf(blk[ti][m][r], f, acc[ti][m][r]);
+              for (int r = 0; r < 4; ++r) acc[m][r] = fmaf(blk[0][m][r] + blk[1][m][r], f, acc[m][r]);
           }
         }
       }
-    }
-
-    // ------------------------------------------------------------ row-block (segment) end
-    // the four K quarters of each row group add up: quarters 1..3 hand their sums to quarter 0
-    if (!lead) {
-      float* xs = xchg + (((rg * (S2_KQ - 1) + (kq - 1)) * S2_TPW) * 32 + lane) * 4 * MT;
-#pragma unroll
-      for (int ti = 0; ti < S2_TPW; ++ti)
+      if constexpr (FMT == FMT_INT8) {
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
-          for (int r = 0; r < 4; ++r)
-            xs[ti * 32 * 4 * MT + m * 4 + r] = kInt ? __int_as_float(acci[ti][m][r]) : acc[ti][m][r];
+          for (int r = 0; r < 4; ++r) acci[m][r] += __float2int_rn(ui[0][m][r] + ui[1][m][r]);
+      }
+      // every shared-memory fragment of the unit has been read: hand the stage back
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[slot]);
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
+      }
     }
-    consumer_sync();
-    float res[S2_TPW][MT][4];
-#pragma unroll
-    for (int ti = 0; ti < S2_TPW; ++ti)
+    left -= seg_units;
+
+    // ------------------------------------------------------------ row-block (segment) end
+    if (!have_colf) {
 #pragma unroll
       for (int m = 0; m < MT; ++m)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) res[ti][m][r] = kInt ? __int_as_float(acci[ti][m][r]) : acc[ti][m][r];
-    if (lead) {
-#pragma unroll
-      for (int q3 = 0; q3 < S2_KQ - 1; ++q3) {
-        const float* xs = xchg + (((rg * (S2_KQ - 1) + q3) * S2_TPW) * 32 + lane) * 4 * MT;
-#pragma unroll
-        for (int ti = 0; ti < S2_TPW; ++ti)
-#pragma unroll
-          for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const float o = xs[ti * 32 * 4 * MT + m * 4 + r];
-              res[ti][m][r] = kInt ? __int_as_float(__float_as_int(res[ti][m][r]) + __float_as_int(o)) : res[ti][m][r] + o;
-            }
-      }
+        for (int e = 0; e < 2; ++e) {
+          const int col = 2 * t + e + 8 * m;
+          colf[m][e] = col < a.M ? a.tokf[col] : 0.f;
+        }
+      have_colf = true;
     }
-    consumer_sync();  // the exchange slots are free again
-    const int kt_end = (int)(seg_end - (int64_t)rb * nk);
+    float res[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) res[m][r] = kInt ? __int_as_float(acci[m][r]) : acc[m][r];
+    const int kt_end = kt;
+    const int seg_rb = rb;
+    rb += 1;  // the next segment (if any) starts a new row block
+    kt = 0;
     if (!(kt0 == 0 && kt_end == nk)) {
-      const int cf = s2_cta_of((int64_t)rb * nk, T, G);
+      const int cf = s2_cta_of((int64_t)seg_rb * nk, T, G);
       if (c == cf) {
         // this CTA settles the block after its last unit (this is its last segment)
 #pragma unroll
-        for (int ti = 0; ti < S2_TPW; ++ti)
+        for (int m = 0; m < MT; ++m)
 #pragma unroll
-          for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) own[ti][m][r] = res[ti][m][r];
-        settle_rb = rb;
+          for (int r = 0; r < 4; ++r) own[m][r] = res[m][r];
+        settle_rb = seg_rb;
         continue;
       }
       // another CTA settles it: store the partial sums, then count in with release order
-      if (lead) {
-        float* pb = a.part + ((int64_t)rb * a.maxseg + (c - cf)) * 16 * S2_ROWS;
+      float* pb = a.part + ((int64_t)seg_rb * a.maxseg + (c - cf)) * 16 * S2_ROWS;
 #pragma unroll
-        for (int ti = 0; ti < S2_TPW; ++ti)
+      for (int m = 0; m < MT; ++m)
 #pragma unroll
-          for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const int col = 2 * t + (r & 1) + 8 * m;
-              const int rl = 16 * (S2_TPW * rg + ti) + g + (r >= 2 ? 8 : 0);
-              pb[col * S2_ROWS + rl] = res[ti][m][r];
-            }
-      }
+        for (int r = 0; r < 4; ++r) {
+          const int col = 2 * t + (r & 1) + 8 * m;
+          const int rl = 16 * w + g + (r >= 2 ? 8 : 0);
+          pb[col * S2_ROWS + rl] = res[m][r];
+        }
       __threadfence();
       consumer_sync();
-      if (threadIdx.x == 0) atomicAdd(&a.tickets[rb], 1u);
+      if (threadIdx.x == 0) atomicAdd(&a.tickets[seg_rb], 1u);
       continue;
     }
     // ------------------------------------------------------------ epilogue (whole row block)
-    if (lead) {
+    float rowf[2] = {1.f, 1.f}, rowb[2] = {0.f, 0.f};
 #pragma unroll
-      for (int ti = 0; ti < S2_TPW; ++ti) {
-        const int row0 = row_g + 16 * ti + g;
-        float rf[2] = {1.f, 1.f}, rbv[2] = {0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int row = min(row0 + 8 * e, a.N - 1);
-          if (kInt) rf[e] = a.w_scale[a.w_scale_len > 1 ? row : 0];
-          if (a.bias) rbv[e] = bf16_bits_to_f32(a.bias[row]);
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int col = 2 * t + (r & 1) + 8 * m;
-            const int row = row0 + (r >= 2 ? 8 : 0);
-            if (row >= a.N || col >= a.M) continue;
-            uint16_t yb;
-            if constexpr (kInt) {
-              const int32_t v = __float_as_int(res[ti][m][r]);
-              if (a.acc_out) a.acc_out[(int64_t)col * a.N + row] = v;
-              yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)v, colf[m][r & 1]), rf[r >> 1]));
-            } else {
-              yb = f32_to_bf16_rn(res[ti][m][r] * colf[m][r & 1]);
-            }
-            if (a.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + rbv[r >> 1]);
-            a.y[(int64_t)col * a.ldy + row] = yb;
-          }
-      }
+    for (int e = 0; e < 2; ++e) {
+      const int row = min(row_w + g + 8 * e, a.N - 1);
+      if (kInt) rowf[e] = a.w_scale[a.w_scale_len > 1 ? row : 0];
+      if (a.bias) rowb[e] = bf16_bits_to_f32(a.bias[row]);
     }
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int col = 2 * t + (r & 1) + 8 * m;
+        const int row = row_w + g + (r >= 2 ? 8 : 0);
+        if (row >= a.N || col >= a.M) continue;
+        uint16_t yb;
+        if constexpr (kInt) {
+          const int32_t v = __float_as_int(res[m][r]);
+          if (a.acc_out) a.acc_out[(int64_t)col * a.N + row] = v;
+          yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)v, colf[m][r & 1]), rowf[r >> 1]));
+        } else {
+          yb = f32_to_bf16_rn(res[m][r] * colf[m][r & 1]);
+        }
+        if (a.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + rowb[r >> 1]);
+        a.y[(int64_t)col * a.ldy + row] = yb;
+      }
   }
 
   // -------------------------------------------------------------- settle the shared block
@@ -522,7 +700,7 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
         unsigned v;
         asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(a.tickets + rb) : "memory");
         if (v >= (unsigned)(count - 1)) break;
-        if (++n > lim) {
+        if (++n > lim || *abort) {
           fail();
           break;
         }
@@ -530,62 +708,68 @@ __global__ void __launch_bounds__(S2_THREADS, 1)
       }
     }
     consumer_sync();
-    if (lead) {
-      const float* pb = a.part + (int64_t)rb * a.maxseg * 16 * S2_ROWS;
-      const int row_g = rb * S2_ROWS + 64 * rg;
+    const float* pb = a.part + (int64_t)rb * a.maxseg * 16 * S2_ROWS;
+    const int row_w = rb * S2_ROWS + 16 * w;
+    float rf[2] = {1.f, 1.f}, rbv[2] = {0.f, 0.f};
 #pragma unroll
-      for (int ti = 0; ti < S2_TPW; ++ti) {
-        const int row0 = row_g + 16 * ti + g;
-        float rf[2] = {1.f, 1.f}, rbv[2] = {0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int row = min(row0 + 8 * e, a.N - 1);
-          if (kInt) rf[e] = a.w_scale[a.w_scale_len > 1 ? row : 0];
-          if (a.bias) rbv[e] = bf16_bits_to_f32(a.bias[row]);
-        }
-        // slot 0 is this CTA (registers); slots 1..count-1 the later CTAs, loaded together
-        float v[MT][4][4];
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int col = 2 * t + (r & 1) + 8 * m;
-            const int rl = 16 * (S2_TPW * rg + ti) + g + (r >= 2 ? 8 : 0);
-            v[m][r][0] = own[ti][m][r];
-#pragma unroll
-            for (int u = 1; u < 4; ++u)
-              v[m][r][u] = (u < count) ? __ldcg(pb + ((int64_t)u * 16 + col) * S2_ROWS + rl) : 0.f;
-          }
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const int col = 2 * t + (r & 1) + 8 * m;
-            const int rl = 16 * (S2_TPW * rg + ti) + g + (r >= 2 ? 8 : 0);
-            float sum = 0.f;
-            int sumi = 0;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              if (kInt) sumi += __float_as_int(v[m][r][u]); else sum += v[m][r][u];
-            }
-            for (int sg = 4; sg < count; ++sg) {  // a row block spread over more than 4 CTAs
-              const float x = __ldcg(pb + ((int64_t)sg * 16 + col) * S2_ROWS + rl);
-              if (kInt) sumi += __float_as_int(x); else sum += x;
-            }
-            const int row = row0 + (r >= 2 ? 8 : 0);
-            if (row >= a.N || col >= a.M) continue;
-            uint16_t yb;
-            if constexpr (kInt) {
-              if (a.acc_out) a.acc_out[(int64_t)col * a.N + row] = sumi;
-              yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)sumi, colf[m][r & 1]), rf[r >> 1]));
-            } else {
-              yb = f32_to_bf16_rn(sum * colf[m][r & 1]);
-            }
-            if (a.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + rbv[r >> 1]);
-            a.y[(int64_t)col * a.ldy + row] = yb;
-          }
-      }
+    for (int e = 0; e < 2; ++e) {
+      const int row = min(row_w + g + 8 * e, a.N - 1);
+      if (kInt) rf[e] = a.w_scale[a.w_scale_len > 1 ? row : 0];
+      if (a.bias) rbv[e] = bf16_bits_to_f32(a.bias[row]);
     }
+    // slot 0 is this CTA (registers); slots 1..count-1 the later CTAs, added in CTA order,
+    // read four slots at a time so the loads of a batch overlap
+    float sum[MT][4];
+    int32_t sumi[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        sum[m][r] = own[m][r];
+        sumi[m][r] = __float_as_int(own[m][r]);
+      }
+    for (int u0 = 1; u0 < count; u0 += 4) {
+      float v[MT][4][4];
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int col = 2 * t + (r & 1) + 8 * m;
+          const int rl = 16 * w + g + (r >= 2 ? 8 : 0);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            v[m][r][u] = (u0 + u < count) ? __ldcg(pb + ((int64_t)(u0 + u) * 16 + col) * S2_ROWS + rl) : 0.f;
+        }
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (u0 + u >= count) break;
+            if (kInt)
+              sumi[m][r] += __float_as_int(v[m][r][u]);
+            else
+              sum[m][r] += v[m][r][u];
+          }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int col = 2 * t + (r & 1) + 8 * m;
+        const int row = row_w + g + (r >= 2 ? 8 : 0);
+        if (row >= a.N || col >= a.M) continue;
+        uint16_t yb;
+        if constexpr (kInt) {
+          if (a.acc_out) a.acc_out[(int64_t)col * a.N + row] = sumi[m][r];
+          yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)sumi[m][r], colf[m][r & 1]), rf[r >> 1]));
+        } else {
+          yb = f32_to_bf16_rn(sum[m][r] * colf[m][r & 1]);
+        }
+        if (a.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + rbv[r >> 1]);
+        a.y[(int64_t)col * a.ldy + row] = yb;
+      }
     if (threadIdx.x == 0) a.tickets[rb] = 0;  // ready for the next call
   }
 }

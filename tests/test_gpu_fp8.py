@@ -51,6 +51,13 @@ def test_fp8_other_block_sizes_and_tails(ql):
     compare(c, run(ql, c, 448, 32, 64), 448, bn=32, bk=64)
 
 
+@pytest.mark.parametrize("M,N,K,bn,bk", [(3, 150, 576, 48, 192), (12, 300, 1120, 128, 320)])
+def test_fp8_block_k_not_power_of_two(ql, M, N, K, bn, bk):
+    # block sizes the persistent kernel does not index by shift take the register kernel
+    c = synth.fp8_block_case(M, N, K, seed=24 + M, block_n=bn, block_k=bk)
+    compare(c, run(ql, c, K, bn, bk), K, bn=bn, bk=bk)
+
+
 def test_fp8_large_activations_no_overflow(ql):
     c = synth.fp8_block_case(2, 128, 256, seed=23)
     c["x"][0] = synth.f32_to_bf16_bits((np.linspace(-1, 1, 256) * 3e6).astype(np.float32))
