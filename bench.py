@@ -71,8 +71,8 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha1()
-    for f in ("skinny.cuh", "kernels_skinny.cu", "kernels_quant.cu", "kernels_moe.cu", "gemm_tcgen05.cu", "tc_ptx.cuh",
-              "common.cuh"):
+    for f in ("skinny2.cuh", "kernels_skinny2.cu", "skinny.cuh", "kernels_skinny.cu", "kernels_quant.cu",
+              "kernels_moe.cu", "gemm_tcgen05.cu", "tc_ptx.cuh", "common.cuh"):
         h.update(open(os.path.join(ROOT, "skinny_gemm_dequant_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:12]
 
@@ -187,7 +187,7 @@ def build_c1(ql, torch, shapes=C1_SHAPES, Ms=C1_MS, name="c1"):
     cfg = {"workload": "INT8 W8A8 skinny GEMM, 27B-class decode shapes (N,K) in "
                        "{(17408,5120),(5120,17408),(10240,5120)} x M in {1,2,4,8,16}",
            "shapes": [list(s) for s in shapes], "M": Ms}
-    return Workload(name, calls, 2 * len(calls), cfg)
+    return Workload(name, calls, len(calls), cfg)  # one fused launch per call
 
 
 def build_c0(ql, torch):
@@ -291,6 +291,14 @@ def build_c4(ql, torch):
 
 
 BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4": build_c4}
+
+_SKINNY = ("skinny2_kernel (one launch per call: activation preparation + weight-streaming GEMM); "
+           "achieved = algorithmic bytes per call / CUDA-event time per call (graphs of 32 back-to-back "
+           "calls), aggregated over the step's calls")
+KERNEL_DESC = {"c0": _SKINNY, "c1": _SKINNY, "c2": _SKINNY,
+               "c3": "MoE launches per call (routing, gate_up, down, combine); bytes of the touched experts / "
+                     "event time per call",
+               "c4": "tcgen05 block-scaled GEMM + its activation-quantisation launch; bytes / event time per call"}
 
 
 # ----------------------------------------------------------------------------- timing
@@ -565,8 +573,7 @@ def main():
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)",
-                "kernel": "per-call layer kernels (activation quant + weight-streaming GEMM), bytes per call / "
-                          "event time per call, aggregated over the step's calls",
+                "kernel": KERNEL_DESC[args.config],
                 "algorithmic_bytes_per_step": tot_b}
     if args.config == "c4":
         fl = sum(c["flops"] for c in wl.calls)

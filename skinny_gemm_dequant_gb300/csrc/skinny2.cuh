@@ -86,7 +86,7 @@ struct S2Traits {
 };
 
 // resident CTAs per SM: more warps per scheduler hide the consumers' dependency chains
-__host__ __device__ constexpr int s2_ctas_per_sm(int mt) { return mt == 1 ? 1 : 1; }
+__host__ __device__ constexpr int s2_ctas_per_sm(int mt) { return mt == 1 ? 2 : 1; }
 
 template <int FMT, int MT>
 __host__ __device__ constexpr uint32_t s2_stage_bytes() {
