@@ -467,6 +467,22 @@ def aggregate(values, op="max"):
     return max(values) if op == "max" else sum(values)
 
 
+def max_over_ranks(ms, dist=None, device="cpu"):
+    """The slowest rank's timed region in ms (every rank gets it): the job is done when its last
+    replica is.  `dist` is torch.distributed with a process group (nccl: device "cuda", gloo: "cpu")."""
+    if dist is None:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step, steps, ms_max, world):
+    """GB/s of the whole job: the bytes all replicas processed / the slowest replica's time."""
+    return world * bytes_per_rank_step * steps / (ms_max * 1e-3) / 1e9
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return
@@ -549,13 +565,10 @@ def main():
     with ClockSampler(local) as clk:
         ms_total = time_steps(graphs, args.steps, torch)
     torch.cuda.synchronize()
-    if pg:
-        t = torch.tensor([ms_total], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, pg, "cuda")
     ms_step = ms_total / args.steps
     peaks = load_peaks()
-    value = ws * wl.bytes_per_step / (ms_step * 1e-3) / 1e9  # GB/s, all ranks
+    value = job_throughput(wl.bytes_per_step, args.steps, ms_total, ws)  # GB/s, all ranks
 
     per_call = time_per_call(wl, torch)
     calls = []
