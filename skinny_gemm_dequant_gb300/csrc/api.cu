@@ -88,9 +88,50 @@ Dense2Layout dense2_layout(int fmt, int64_t Mc, int64_t N, int64_t K, int block_
   Carver c;
   l.x16 = c.take((size_t)kXCopies * Mc * l.p.kpad * 2);
   l.sc = c.take(16 * 4);
-  l.part = c.take((size_t)l.p.nb * l.p.maxseg * 16 * S2_ROWS * 4);
+  l.part = c.take((size_t)l.p.grid * 16 * S2_ROWS * 4);  // one partial slot per CTA
   l.total = c.off;
   return l;
+}
+
+// MoE on the persistent kernel: the router's outputs, gate/up sums, expert outputs, the
+// activation image of either stage, per-row factors and per-CTA partial sums
+struct Moe2Layout {
+  Skinny2Plan gu, dn;
+  int slots, slot_rows;
+  size_t ids, wts, offsets, pairs, uniq, nuniq, gus, o, x16, tokf, part, total;
+};
+
+Moe2Layout moe2_layout(int64_t M, int64_t H, int64_t I, int E, int topk) {
+  Moe2Layout l;
+  const int64_t P = M * topk;
+  l.slots = (int)(P < E ? P : E);
+  l.gu = skinny2_plan(FMT_MXFP4, M, 2 * I, H, 0, l.slots);
+  l.dn = skinny2_plan(FMT_MXFP4, M, H, I, 0, l.slots);
+  l.slot_rows = l.dn.mp;
+  Carver c;
+  l.ids = c.take(P * 4);
+  l.wts = c.take(P * 4);
+  l.offsets = c.take((E + 1) * 4);
+  l.pairs = c.take(P * 4);
+  l.uniq = c.take((size_t)E * 4);
+  l.nuniq = c.take(4);
+  l.gus = c.take((size_t)P * 2 * I * 4);
+  l.o = c.take((size_t)P * H * 4);
+  const size_t img_gu = (size_t)kXCopies * M * l.gu.kpad * 2;
+  const size_t img_dn = (size_t)kXCopies * l.slots * l.slot_rows * l.dn.kpad * 2;
+  l.x16 = c.take(img_gu > img_dn ? img_gu : img_dn);
+  l.tokf = c.take((size_t)(l.slots * l.slot_rows > M ? l.slots * l.slot_rows : M) * 4);
+  const int g = l.gu.grid > l.dn.grid ? l.gu.grid : l.dn.grid;
+  l.part = c.take((size_t)g * 16 * S2_ROWS * 4);
+  l.total = c.off;
+  return l;
+}
+
+// the persistent kernel takes the MoE when both K's are whole 256-K units (scale rows then
+// whole 8-byte groups) and the scale arrays are 8-byte aligned
+bool moe2_ok(int64_t H, int64_t I, const void* s13, const void* s2) {
+  return H % 256 == 0 && I % 256 == 0 && (reinterpret_cast<uintptr_t>(s13) & 7) == 0 &&
+         (reinterpret_cast<uintptr_t>(s2) & 7) == 0;
 }
 
 // MXFP4 weights go through the persistent kernel when whole 256-K units and 8-byte scale
@@ -180,6 +221,7 @@ ql_status run_dense2(const Dense2Call& d, void* workspace, cudaStream_t st) {
     a.ldx = d.ldx;
     a.x16 = at<uint16_t>(workspace, l.x16);
     a.tokf = at<float>(workspace, l.sc);
+    a.img_rows = (int)Mc;
     a.xq_dbg = d.xq_out ? d.xq_out + m0 * d.K : nullptr;
     a.xs_dbg = d.xs_out ? d.xs_out + m0 : nullptr;
     a.ready = at<unsigned>(workspace, kReadyOff);
@@ -245,9 +287,11 @@ size_t ql_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int to
       const size_t b = act_quant_ws(M, K);
       return a > b ? a : b;
     }
-    case QL_OP_MOE_MXFP4:
+    case QL_OP_MOE_MXFP4: {
       if (E <= 0 || topk <= 0) return 0;
-      return moe_layout(M, N, K, E, topk).total;
+      const size_t a = moe_layout(M, N, K, E, topk).total, b = moe2_layout(M, N, K, E, topk).total;
+      return a > b ? a : b;
+    }
   }
   return 0;
 }
@@ -500,6 +544,76 @@ ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint1
   if (!workspace || workspace_bytes < ql_workspace_bytes(QL_OP_MOE_MXFP4, M, H, I, E, topk)) return QL_ERR_WORKSPACE;
   if (!al16(workspace)) return QL_ERR_ALIGNMENT;
   cudaStream_t st = (cudaStream_t)stream;
+  if (moe2_ok(H, I, s13, s2)) {
+    const Moe2Layout l = moe2_layout(M, H, I, E, topk);
+    if ((int64_t)l.slots * (l.gu.nb > l.dn.nb ? l.gu.nb : l.dn.nb) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
+    MoeRouteArgs r = {};
+    r.logits = router_logits;
+    r.ids_in = topk_ids_in;
+    r.w_in = topk_w_in;
+    r.M = (int)M;
+    r.E = E;
+    r.topk = topk;
+    r.renorm = renormalize;
+    r.ids = at<int32_t>(workspace, l.ids);
+    r.wts = at<float>(workspace, l.wts);
+    r.offsets = at<int32_t>(workspace, l.offsets);
+    r.pairs = at<int32_t>(workspace, l.pairs);
+    r.uniq = at<int32_t>(workspace, l.uniq);
+    r.nuniq = at<int32_t>(workspace, l.nuniq);
+    r.ids_dbg = topk_ids_out;
+    r.w_dbg = topk_w_out;
+    r.status = at<uint32_t>(workspace, 0);
+    cudaError_t e = launch_moe_route(r, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    Skinny2Args a = {};
+    a.x16 = at<uint16_t>(workspace, l.x16);
+    a.tokf = at<float>(workspace, l.tokf);
+    a.ready = at<unsigned>(workspace, kReadyOff);
+    a.done = at<unsigned>(workspace, kDoneOff);
+    a.part = at<float>(workspace, l.part);
+    a.tickets = at<unsigned>(workspace, kTicketOff);
+    a.status = at<uint32_t>(workspace, 0);
+    a.wait_limit = g_wait_limit;
+    a.nuniq = r.nuniq;
+    a.uniq = r.uniq;
+    a.offsets = r.offsets;
+    a.pairs = r.pairs;
+    a.ids = r.ids;
+    a.topk = topk;
+    a.E = E;
+    a.I = (int)I;
+    a.gu = at<float>(workspace, l.gus);
+    a.slot_rows = l.slot_rows;
+    a.M = (int)M;
+    // stage 1: gate and up rows of W13[e] against every token's x
+    a.N = (int)(2 * I);
+    a.K = (int)H;
+    a.x = x;
+    a.ldx = H;
+    a.img_rows = (int)M;
+    a.wsb = s13;
+    a.lds = H / 32;
+    a.s_estride = 2 * I * (H / 32);
+    e = launch_moe2(S2_MOE_GU, l.gu, a, w13, H / 2, 2 * I * (H / 2), E, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    // stage 2: rows of W2[e] against the gathered h = bf16(silu(g) * u) of its pairs
+    a.N = (int)H;
+    a.K = (int)I;
+    a.x = nullptr;
+    a.img_rows = l.slots * l.slot_rows;
+    a.wsb = s2;
+    a.lds = I / 32;
+    a.s_estride = H * (I / 32);
+    a.h_dbg = h_out;
+    a.o = at<float>(workspace, l.o);
+    e = launch_moe2(S2_MOE_DN, l.dn, a, w2, I / 2, H * (I / 2), E, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    e = launch_moe_combine(a.o, r.ids, r.wts, (int)M, topk, (int)H, y, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (path_out) *path_out = QL_PATH_MOE_MXFP4;
+    return QL_OK;
+  }
   const MoeLayout l = moe_layout(M, H, I, E, topk);
   if ((int64_t)l.umax * (l.nb_gu > l.nb_dn ? l.nb_gu : l.nb_dn) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
 

@@ -46,14 +46,16 @@ struct Skinny2Plan {
   int64_t kpad;           // K rounded up to whole units (row length of the activation image)
   int64_t total;          // nb * nk
   int grid;               // CTAs (one per SM)
-  int maxseg;             // partial slots per row block
   int64_t units_per_cta;
   size_t fp8_scale_bytes; // shared memory for the FP8 block-scale rows
 };
-Skinny2Plan skinny2_plan(int fmt, int64_t M, int64_t N, int64_t K, int block_n);
+Skinny2Plan skinny2_plan(int fmt, int64_t M, int64_t N, int64_t K, int block_n, int64_t slots = 1);
 struct Skinny2Args;
 cudaError_t launch_skinny2(int fmt, const Skinny2Plan& p, const Skinny2Args& a, const uint8_t* w, int64_t ldw,
                            cudaStream_t st);
+// the two MXFP4 expert GEMVs of the MoE (kind: S2_MOE_GU or S2_MOE_DN, skinny2.cuh)
+cudaError_t launch_moe2(int kind, const Skinny2Plan& p, const Skinny2Args& a, const uint8_t* w, int64_t ldw,
+                        int64_t w_estride, int experts, cudaStream_t st);
 
 // split-K choice of the skinny kernel (shared by the workspace query and the launch)
 struct SplitK {

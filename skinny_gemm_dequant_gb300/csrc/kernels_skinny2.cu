@@ -1,17 +1,20 @@
-// Plan and launch of the persistent TMA-fed skinny GEMM (skinny2.cuh): work split, tensor maps
-// of the weights and of the activation image, shared-memory ring depth.
+// Plan and launch of the persistent TMA-fed skinny GEMM (skinny2_kernel.cuh): work split, tensor
+// maps of the weights and of the activation image, shared-memory ring depth.  Dense linear layers
+// and the two MXFP4 expert GEMVs of the MoE go through the same kernel.
 #include <atomic>
 
 #include <cudaTypedefs.h>
 
 #include "internal.h"
-#include "skinny2.cuh"
+#include "skinny2_kernel.cuh"
 
 namespace ql {
 
 // ------------------------------------------------------------------ plan + launch
 
-Skinny2Plan skinny2_plan(int fmt, int64_t M, int64_t N, int64_t K, int block_n) {
+// slots: 1 for a dense layer; for the MoE the most distinct experts a call can route to (the
+// device knows the actual count and splits the units by it)
+Skinny2Plan skinny2_plan(int fmt, int64_t M, int64_t N, int64_t K, int block_n, int64_t slots) {
   Skinny2Plan p;
   p.mt = M <= 8 ? 1 : 2;
   p.mp = 8 * p.mt;
@@ -19,18 +22,9 @@ Skinny2Plan skinny2_plan(int fmt, int64_t M, int64_t N, int64_t K, int block_n) 
   p.nb = (N + S2_ROWS - 1) / S2_ROWS;
   p.nk = (int)((K + kpu - 1) / kpu);
   p.kpad = (int64_t)p.nk * kpu;
-  p.total = p.nb * p.nk;
+  p.total = slots * p.nb * p.nk;
   const int64_t sms = (int64_t)kNumSMs * s2_ctas_per_sm(p.mt);  // fixed: workspace query and launch agree
   p.grid = (int)(p.total < sms ? p.total : sms);
-  // partial slots: the most CTAs any row block is spread over
-  int maxseg = 1;
-  for (int64_t rb = 0; rb < p.nb; ++rb) {
-    const int64_t a = rb * p.nk, b = rb * p.nk + p.nk - 1;
-    const int64_t ca = ((a + 1) * p.grid + p.total - 1) / p.total - 1;
-    const int64_t cb = ((b + 1) * p.grid + p.total - 1) / p.total - 1;
-    if (cb - ca + 1 > maxseg) maxseg = (int)(cb - ca + 1);
-  }
-  p.maxseg = maxseg;
   p.units_per_cta = (p.total + p.grid - 1) / p.grid;
   p.fp8_scale_bytes = 0;
   if (fmt == FMT_FP8) {
@@ -86,8 +80,10 @@ static bool map2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, int MT>
-static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w, int64_t ldw, cudaStream_t st) {
+// w_estride: bytes between experts' weight matrices (MoE; a dense layer has one "expert")
+template <int FMT, int MT, int KIND>
+static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w, int64_t ldw, int64_t w_estride,
+                           int experts, cudaStream_t st) {
   using Tr = S2Traits<FMT>;
   constexpr uint32_t STAGE = s2_stage_bytes<FMT, MT>();
   constexpr int Mp = 8 * MT;
@@ -101,31 +97,34 @@ static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w
   a.bk_shift = 0;
   while (a.block_k > 0 && (1 << a.bk_shift) < a.block_k) ++a.bk_shift;
   a.nk = p.nk;
+  a.nb = (int)p.nb;
   a.total = p.total;
-  a.maxseg = p.maxseg;
   const uint64_t wbytes = FMT == FMT_MXFP4 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
   a.wbytes = (int)wbytes;
   const size_t smem = 1024 + (size_t)S * STAGE + (size_t)S * 16 + p.fp8_scale_bytes;
   CUtensorMap tw, tw2, tx;
-  // whole 128-byte chunks as the third dimension: a box of 2 chunks is one 32 KB TMA operation
+  // whole 128-byte chunks as the third dimension (a box of 2 chunks is one 32 KB TMA operation),
+  // experts as the fourth
   const uint64_t nfull = wbytes / 128 > 0 ? wbytes / 128 : 1;
   {
-    const uint64_t d[3] = {128, (uint64_t)a.N, nfull}, st[2] = {(uint64_t)ldw, 128};
-    const uint32_t b[3] = {128, S2_ROWS, S2_CHUNKS};
-    if (!mapnd(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, 3, d, st, b)) return cudaErrorInvalidValue;
+    const uint64_t d[4] = {128, (uint64_t)a.N, nfull, (uint64_t)experts};
+    const uint64_t st[3] = {(uint64_t)ldw, 128, (uint64_t)w_estride};
+    const uint32_t b[4] = {128, S2_ROWS, S2_CHUNKS, 1};
+    if (!mapnd(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, 4, d, st, b)) return cudaErrorInvalidValue;
   }
   if (!map2d(&tw2, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, wbytes, (uint64_t)a.N, (uint64_t)ldw, 128, S2_ROWS))
     return cudaErrorInvalidValue;
   a.xcopies = kXCopies;
   a.kpad = p.kpad;
   {
-    // image [copies][M][kpad] f16 seen as {64, M, copies, kpad/64}; a box covers Mp >= M rows
-    const uint64_t d[4] = {64, (uint64_t)a.M, (uint64_t)kXCopies, (uint64_t)(p.kpad / 64)};
-    const uint64_t st[3] = {(uint64_t)p.kpad * 2, (uint64_t)a.M * p.kpad * 2, 128};
+    // image [copies][img_rows][kpad] f16 seen as {64, img_rows, copies, kpad/64}; a box covers
+    // Mp rows (rows past img_rows read as zeros)
+    const uint64_t d[4] = {64, (uint64_t)a.img_rows, (uint64_t)kXCopies, (uint64_t)(p.kpad / 64)};
+    const uint64_t st[3] = {(uint64_t)p.kpad * 2, (uint64_t)a.img_rows * p.kpad * 2, 128};
     const uint32_t b[4] = {64, (uint32_t)Mp, 1, (uint32_t)Tr::NXB};
     if (!mapnd(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.x16, 4, d, st, b)) return cudaErrorInvalidValue;
   }
-  auto kfn = skinny2_kernel<FMT, MT>;
+  auto kfn = skinny2_kernel<FMT, MT, KIND>;
   static std::atomic<int> attr{0};
   if (!attr.load()) {
     cudaError_t e = raise_smem_limit(kfn);
@@ -147,9 +146,24 @@ static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w
 
 cudaError_t launch_skinny2(int fmt, const Skinny2Plan& p, const Skinny2Args& a, const uint8_t* w, int64_t ldw,
                            cudaStream_t st) {
-  if (fmt == FMT_INT8) return p.mt == 1 ? launch2<FMT_INT8, 1>(p, a, w, ldw, st) : launch2<FMT_INT8, 2>(p, a, w, ldw, st);
-  if (fmt == FMT_FP8) return p.mt == 1 ? launch2<FMT_FP8, 1>(p, a, w, ldw, st) : launch2<FMT_FP8, 2>(p, a, w, ldw, st);
-  return p.mt == 1 ? launch2<FMT_MXFP4, 1>(p, a, w, ldw, st) : launch2<FMT_MXFP4, 2>(p, a, w, ldw, st);
+  const int64_t es = (int64_t)a.N * ldw;  // one expert
+  if (fmt == FMT_INT8)
+    return p.mt == 1 ? launch2<FMT_INT8, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
+                     : launch2<FMT_INT8, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);
+  if (fmt == FMT_FP8)
+    return p.mt == 1 ? launch2<FMT_FP8, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
+                     : launch2<FMT_FP8, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);
+  return p.mt == 1 ? launch2<FMT_MXFP4, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
+                   : launch2<FMT_MXFP4, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);
+}
+
+cudaError_t launch_moe2(int kind, const Skinny2Plan& p, const Skinny2Args& a, const uint8_t* w, int64_t ldw,
+                        int64_t w_estride, int experts, cudaStream_t st) {
+  if (kind == S2_MOE_GU)
+    return p.mt == 1 ? launch2<FMT_MXFP4, 1, S2_MOE_GU>(p, a, w, ldw, w_estride, experts, st)
+                     : launch2<FMT_MXFP4, 2, S2_MOE_GU>(p, a, w, ldw, w_estride, experts, st);
+  return p.mt == 1 ? launch2<FMT_MXFP4, 1, S2_MOE_DN>(p, a, w, ldw, w_estride, experts, st)
+                   : launch2<FMT_MXFP4, 2, S2_MOE_DN>(p, a, w, ldw, w_estride, experts, st);
 }
 
 }  // namespace ql

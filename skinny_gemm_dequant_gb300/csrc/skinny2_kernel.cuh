@@ -1,0 +1,559 @@
+// The persistent skinny GEMM kernel (layout, helpers and activation jobs: skinny2.cuh).
+//
+// One kernel serves three kinds of launch:
+//  * S2_DENSE: y = dequant(W) x for INT8 / FP8-block / MXFP4 weights (M <= 16 tokens);
+//  * S2_MOE_GU: MoE stage 1, for every distinct routed expert e the gate and up rows of W13[e]
+//    against all M tokens' activations (the MMA's 8 or 16 token columns cost the same however
+//    many are routed); the epilogue keeps the (token, e) pairs the router chose and stores their
+//    raw sums gu[pair] in fp32;
+//  * S2_MOE_DN: MoE stage 2, for every distinct expert the rows of W2[e] against the gathered
+//    rows h = bf16(silu(g) * u) of its pairs (prepared by this kernel's activation jobs from
+//    gu); the epilogue stores o[pair] in fp32 for the weighted combine.
+// For the MoE kinds a unit is (expert slot, 128-row block, 256 weight bytes of K); the slots are
+// the router's distinct experts, so the unit count is read on the device after the
+// grid-dependency wait and split evenly over the CTAs there.
+#pragma once
+#include "skinny2.cuh"
+
+namespace ql {
+
+// tmW: 4D view {128 bytes, N rows, full 128-byte chunks, experts} (strides ldw, 128, expert
+//      stride), box {128, 128, 2, 1}
+// tmW2: 2D view {wbytes, N}, box {128, 128}: dense units holding a partial chunk
+// tmX: 4D view of the activation image {64 f16, img_rows, copies, kpad/64}, box {64, Mp, 1, NXB}
+//      (rows past img_rows read as zeros)
+template <int FMT, int MT, int KIND>
+__global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
+    skinny2_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
+                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Skinny2Args a) {
+  using Tr = S2Traits<FMT>;
+  constexpr int Mp = 8 * MT;
+  constexpr uint32_t W_CHUNK = S2_ROWS * 128;  // one 128-byte chunk of all 128 rows (16 KB)
+  constexpr uint32_t W_BYTES = W_CHUNK * S2_CHUNKS;
+  constexpr uint32_t X_BOX = Mp * 128;         // one 64-element slab of all token rows
+  constexpr uint32_t X_BYTES = Tr::NXB * X_BOX;
+  constexpr uint32_t STAGE = s2_stage_bytes<FMT, MT>();
+  constexpr bool kInt = (FMT == FMT_INT8);
+  constexpr bool kMoE = (KIND != S2_DENSE);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = a.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * STAGE);
+  uint64_t* empty = full + S;
+  uint8_t* fp8sc = reinterpret_cast<uint8_t*>(empty + S);  // FP8 scale rows of this CTA's row blocks
+  __shared__ int s_abort;
+
+  // the next kernel in the stream may launch now: it waits for this grid before it touches
+  // memory, and meanwhile can take each SM this grid leaves and start streaming its weights
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  // MoE: the units follow the router's distinct experts (the kernel before this one)
+  int nu = 1;
+  if constexpr (kMoE) {
+    pdl_wait();
+    nu = min(*a.nuniq, a.E);
+  }
+  const int64_t T = kMoE ? (int64_t)nu * a.nb * a.nk : a.total;
+  const int64_t s0 = (int64_t)c * T / G, s1 = (int64_t)(c + 1) * T / G;
+  const int nk = a.nk;
+  const uint32_t lim = a.wait_limit;
+  volatile int* abort = &s_abort;
+  auto fail = [&]() {
+    atomicOr(a.status, (uint32_t)QL_DEV_TIMEOUT);
+    *abort = 1;
+  };
+  // jobs that build the activation image, and how many of them the producers wait for
+  const int njob_rows = KIND == S2_MOE_DN ? a.offsets[a.E] : a.M;
+  const int nsl = s2_slices(max(njob_rows, 1), G);
+  const unsigned need = (unsigned)(njob_rows * nsl);
+
+  const int rb_first = (int)(s0 / nk);  // global row block (expert slot * nb + block)
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(&full[i], FMT == FMT_MXFP4 ? 1 + 32 : 1);
+      tc::mbar_init(&empty[i], S2_CONSUMERS);
+    }
+    tc::fence_mbar_init();
+    s_abort = 0;
+    tc::tma_prefetch_desc(&tmW);
+    tc::tma_prefetch_desc(&tmX);
+  }
+  if constexpr (FMT == FMT_FP8) {  // dense only: the block-scale rows of this CTA's row blocks
+    const int nbr = S2_ROWS / a.block_n + 2;  // n-blocks a 128-row block can touch
+    const int rb_last = (int)((s1 - 1) / nk);
+    const int nrow_blocks = rb_last - rb_first + 1;
+    const int nb0 = (rb_first * S2_ROWS) / a.block_n;
+    const int nb_count = min(nrow_blocks * nbr, (int)((a.N + a.block_n - 1) / a.block_n) - nb0);
+    for (int i = threadIdx.x; i < nb_count * a.lds; i += blockDim.x) fp8sc[i] = a.wsb[(int64_t)nb0 * a.lds + i];
+  }
+  __syncthreads();
+
+  if (warp == S2_CONSUMERS) {
+    // ------------------------------------------------------------ producer warp
+    const int n_units = (int)(s1 - s0);
+    const int pre = min(S, n_units);
+    const int xcp = c % a.xcopies;  // this CTA's copy of the activation image
+    const bool whole_chunks = (a.wbytes & 127) == 0;
+    const int ksc = a.K / 32;  // MXFP4 scale bytes of a row that belong to K
+    // the activation hand-off: wait (bounded) until the image is complete, count in (the last
+    // producer returns both counters to zero for the next call) and report whether it timed out
+    auto handoff = [&]() {
+      pdl_wait();  // the counters belong to the previous call until its grid is done
+      for (uint32_t n = 0;; ++n) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(a.ready) : "memory");
+        if (v >= need) break;
+        if (n >= lim) {
+          fail();
+          break;
+        }
+        __nanosleep(32);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // generic writes -> TMA reads
+      if (atomicAdd(a.done, 1u) == (unsigned)G - 1) {
+        *a.ready = 0;
+        *a.done = 0;
+      }
+    };
+    if (n_units == 0) {
+      if (lane == 0) handoff();
+      return;
+    }
+    bool ok = true;
+    int issued = 0;
+    // unit counters kept incrementally: no divisions in the loop
+    int rb = rb_first, kt = (int)(s0 - (int64_t)rb_first * nk);
+    int u = kMoE ? rb / a.nb : 0, rbl = rb - u * a.nb;  // expert slot, block within the expert
+    int ex = kMoE ? a.uniq[u] : 0;                      // expert
+    int slot = 0;
+    uint32_t phase = 0;  // (i / S) & 1
+    for (int i = 0; i < n_units; ++i) {
+      int got = 1;
+      if (lane == 0 && i >= S) got = tc::mbar_wait(&empty[slot], phase ^ 1u, lim, abort);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) {
+        if (lane == 0) fail();
+        ok = false;
+        break;
+      }
+      const uint32_t st = tc::smem_u32(smem + (size_t)slot * STAGE);
+      const int xrow = KIND == S2_MOE_DN ? u * a.slot_rows : 0;  // first image row of this unit
+      if (lane == 0) {
+        // weights: chunks 2kt, 2kt+1 of rows rbl*128.. of expert ex -> smem [chunk][row][128 B]
+        if (whole_chunks || (kt + 1) * S2_WB <= a.wbytes) {
+          tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + X_BYTES);
+          tma_load_4d(st, &tmW, 0, rbl * S2_ROWS, kt * S2_CHUNKS, ex, &full[slot]);
+        } else {
+          // the row ends inside this unit, off a chunk boundary: a chunk at a time from the 2D
+          // view, whose bytes past the end (a whole chunk, possibly) are filled with zeros
+          tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + X_BYTES);
+          tc::tma_load_2d(smem + (size_t)slot * STAGE, &tmW2, kt * S2_WB, rbl * S2_ROWS, &full[slot]);
+          tc::tma_load_2d(smem + (size_t)slot * STAGE + W_CHUNK, &tmW2, kt * S2_WB + 128, rbl * S2_ROWS, &full[slot]);
+        }
+        if (i >= pre) {
+          tma_load_4d(st + W_BYTES, &tmX, 0, xrow, xcp, kt * Tr::NXB, &full[slot]);
+        } else if (i == pre - 1) {
+          // the activation image is written by this grid's consumer warps: wait for it, then
+          // load the activation tiles of the stages already in flight.  On a timeout the
+          // status is flagged and the loads still go out, so no stage waits forever.
+          handoff();
+          int ktj = (int)(s0 - (int64_t)rb_first * nk), rbj = rb_first;
+          for (int j = 0; j < pre; ++j) {  // pre <= S: stage j is slot j
+            const int uj = kMoE ? rbj / a.nb : 0;
+            const uint32_t stj = tc::smem_u32(smem + (size_t)j * STAGE);
+            tma_load_4d(stj + W_BYTES, &tmX, 0, KIND == S2_MOE_DN ? uj * a.slot_rows : 0, xcp, ktj * Tr::NXB,
+                        &full[j]);
+            if (++ktj == nk) {
+              ktj = 0;
+              ++rbj;
+            }
+          }
+        }
+      }
+      if constexpr (FMT == FMT_MXFP4) {
+        // per-32 scale bytes of the unit: 128 rows x (8 bytes per chunk); bytes past K read as 0
+        const uint32_t sc = st + W_BYTES + X_BYTES;
+        const uint8_t* sbase = a.wsb + (int64_t)ex * a.s_estride;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = lane * 4 + (j >> 1), h = j & 1;
+          const int n = min(rbl * S2_ROWS + r, a.N - 1);
+          const int b0 = kt * 16 + h * 8;
+          cp_async8(sc + r * 16 + h * 8, sbase + (int64_t)n * a.lds + (b0 < ksc ? b0 : 0), b0 < ksc ? 8u : 0u);
+        }
+        cp_async_mbar_arrive(&full[slot]);
+      }
+      issued = i + 1;
+      if (++kt == nk) {
+        kt = 0;
+        ++rb;
+        if (++rbl == a.nb) {
+          rbl = 0;
+          ++u;
+          if (kMoE && u < nu) ex = a.uniq[u];
+        }
+      }
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok && lane == 0) {
+      // no copy may land after the CTA exits: wait for every stage still in flight
+      for (int i = max(0, issued - S); i < issued; ++i)
+        tc::mbar_wait(&full[i % S], (uint32_t)(i / S) & 1, 1u << 22, nullptr);
+    }
+    if constexpr (FMT == FMT_MXFP4) asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
+  // -------------------------------------------------------------- consumer warps
+  // activations may come from the previous kernel in the stream: wait for it, then write this
+  // CTA's jobs of the activation image (jobs j = c, c + G, ... of rows x slices), count them in
+  pdl_wait();
+  {
+    __shared__ float s_red[S2_CONSUMERS];
+    unsigned mine = 0;
+    for (int j = c; j < njob_rows * nsl; j += G, ++mine) {
+      if constexpr (KIND == S2_MOE_DN)
+        s2_prepare_h(a, j % njob_rows, j / njob_rows, nsl, nu, threadIdx.x, s_red);
+      else
+        s2_prepare<FMT>(a, j % njob_rows, j / njob_rows, nsl, threadIdx.x, s_red);
+    }
+    if (mine) {
+      // the rows are read by TMA (async proxy) in other CTAs: proxy fence, then one release
+      // (cumulative over the CTA's writes, ordered before it by the barrier)
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      consumer_sync();
+      if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a.ready), "r"(mine) : "memory");
+    }
+  }
+  const int g = lane >> 2, t = lane & 3;
+  const int w = warp;  // 16-row tile of the unit
+  // ldmatrix addressing: lane L feeds row 16w + (L & 7) + 8*((L >> 3) & 1) of piece 2p + (L >> 4)
+  const int lrow = 16 * w + (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int lpc = lane >> 4;
+
+  // one complete row block's results (fp32 sums, or int32 bits for INT8) to their outputs.  The
+  // per-token factors (x_s or 2^p) are read here: a stage has arrived by then, and activations
+  // were loaded only after the image, factors included, was complete.
+  auto emit = [&](int grb, const float (&res)[MT][4]) {
+    const int eu = kMoE ? grb / a.nb : 0;  // expert slot
+    const int row_w = (grb - eu * a.nb) * S2_ROWS + 16 * w;
+    const int ex = kMoE ? a.uniq[eu] : 0;
+    int beg = 0, cnt = a.M;  // MoE down: the expert's pairs are dispatch positions beg..beg+cnt-1
+    if constexpr (KIND == S2_MOE_DN) {
+      beg = a.offsets[ex];
+      cnt = min(a.offsets[ex + 1] - beg, a.slot_rows);
+    }
+    float colf[MT][2];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int col = 2 * t + e2 + 8 * m;
+        colf[m][e2] = col < cnt ? a.tokf[(KIND == S2_MOE_DN ? eu * a.slot_rows : 0) + col] : 0.f;
+      }
+    float rowf[2] = {1.f, 1.f}, rowb[2] = {0.f, 0.f};
+    if constexpr (KIND == S2_DENSE) {
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int row = min(row_w + g + 8 * e2, a.N - 1);
+        if (kInt) rowf[e2] = a.w_scale[a.w_scale_len > 1 ? row : 0];
+        if (a.bias) rowb[e2] = bf16_bits_to_f32(a.bias[row]);
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int col = 2 * t + (r & 1) + 8 * m;
+        const int row = row_w + g + (r >= 2 ? 8 : 0);
+        if (row >= a.N || col >= cnt) continue;
+        if constexpr (KIND == S2_MOE_GU) {
+          // keep the sums of the pair (token col, expert ex), if the router chose it
+          int p = -1;
+          for (int k = 0; k < a.topk; ++k)
+            if (a.ids[col * a.topk + k] == ex) p = col * a.topk + k;
+          if (p >= 0) a.gu[(int64_t)p * a.N + row] = res[m][r] * colf[m][r & 1];
+        } else if constexpr (KIND == S2_MOE_DN) {
+          a.o[(int64_t)a.pairs[beg + col] * a.N + row] = res[m][r] * colf[m][r & 1];
+        } else {
+          uint16_t yb;
+          if constexpr (kInt) {
+            const int32_t v = __float_as_int(res[m][r]);
+            if (a.acc_out) a.acc_out[(int64_t)col * a.N + row] = v;
+            yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)v, colf[m][r & 1]), rowf[r >> 1]));
+          } else {
+            yb = f32_to_bf16_rn(res[m][r] * colf[m][r & 1]);
+          }
+          if (a.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + rowb[r >> 1]);
+          a.y[(int64_t)col * a.ldy + row] = yb;
+        }
+      }
+  };
+
+  float acc[MT][4];
+  int32_t acci[MT][4];
+  float own[MT][4];  // partial sums of the block this CTA settles
+  int settle_rb = -1;
+  bool ok = true;
+  int rb = rb_first;
+  int kt = (int)(s0 - (int64_t)rb_first * nk);
+  int slot = 0;
+  uint32_t phase = 0;
+  int left = (int)(s1 - s0);  // units still to consume
+  while (left > 0) {
+    const int kt0 = kt;
+    const int seg_units = min(nk - kt, left);  // this row block's units in the range
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        acc[m][r] = 0.f;
+        acci[m][r] = 0;
+      }
+    const uint8_t* sc_row = nullptr;  // FP8 (dense): scale row of this warp's n-block
+    if constexpr (FMT == FMT_FP8) {
+      const int nb = min(rb * S2_ROWS + 16 * w, a.N - 1) / a.block_n;
+      sc_row = fp8sc + (int64_t)(nb - (rb_first * S2_ROWS) / a.block_n) * a.lds;
+    }
+    for (int u = 0; u < seg_units; ++u, ++kt) {
+      int got = 0;
+      if (lane == 0 && ok) got = tc::mbar_wait(&full[slot], phase, lim, abort);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) {
+        // timed out (or another role did): stop computing but keep walking the units, so
+        // every consumer warp still reaches the same named barriers below
+        if (lane == 0 && ok) fail();
+        ok = false;
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1u;
+        }
+        continue;
+      }
+      const uint32_t st = tc::smem_u32(smem + (size_t)slot * STAGE);
+      const uint32_t xt = st + W_BYTES;
+      // INT8: the unit's sums in two fp32 chains; every partial sum is an integer of at most
+      // 256 x 127 x 127 < 2^24 in magnitude, so they are exact and convert once per unit
+      float ui[2][MT][4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) ui[e][m][0] = ui[e][m][1] = ui[e][m][2] = ui[e][m][3] = 0.f;
+#pragma unroll
+      for (int ck = 0; ck < S2_CHUNKS; ++ck) {
+        const uint32_t wt = st + ck * W_CHUNK;
+        // the chunk's 8 sixteen-byte pieces for this warp's 16 rows (4 ldmatrix.x4):
+        // q[p] = (row g, piece 2p), (g+8, 2p), (g, 2p+1), (g+8, 2p+1)
+        uint32_t q[4][4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          ldmatrix_x4(wt + sw128(lrow, (2 * p + lpc) * 16), q[p][0], q[p][1], q[p][2], q[p][3]);
+        if constexpr (FMT == FMT_MXFP4) {
+          // scale bytes of rows g and g+8 for the chunk's 8 groups
+          const uint32_t sbase = st + W_BYTES + X_BYTES;
+          const uint2 sa8 = lds64(sbase + (16 * w + g) * 16 + ck * 8);
+          const uint2 sb8 = lds64(sbase + (16 * w + g + 8) * 16 + ck * 8);
+#pragma unroll
+          for (int pc = 0; pc < 8; ++pc) {  // piece = one 32-element scale group
+            const uint32_t qa = q[pc >> 1][2 * (pc & 1)], qb = q[pc >> 1][2 * (pc & 1) + 1];
+            // this thread's 8 weights of the piece are K 8t..8t+7: the activations of those
+            // K are 16 contiguous bytes of the token's row
+            const int kx = 32 * pc + 8 * t;  // K within the chunk
+            uint4 xv[MT];
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+              xv[m] = lds128(xt + (4 * ck + (kx >> 6)) * X_BOX + sw128(g + 8 * m, (kx & 63) * 2));
+            float blk[MT][4];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) blk[m][0] = blk[m][1] = blk[m][2] = blk[m][3] = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t a0 = e2m1x2_to_f16x2(qa >> (16 * h));
+              const uint32_t a2 = e2m1x2_to_f16x2(qa >> (16 * h + 8));
+              const uint32_t a1 = e2m1x2_to_f16x2(qb >> (16 * h));
+              const uint32_t a3 = e2m1x2_to_f16x2(qb >> (16 * h + 8));
+#pragma unroll
+              for (int m = 0; m < MT; ++m)
+                mma_f16_16816(blk[m], a0, a1, a2, a3, h ? xv[m].z : xv[m].x, h ? xv[m].w : xv[m].y);
+            }
+            const float fa = ue8m0_to_f32((pc < 4 ? sa8.x : sa8.y) >> (8 * (pc & 3)));
+            const float fb = ue8m0_to_f32((pc < 4 ? sb8.x : sb8.y) >> (8 * (pc & 3)));
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              acc[m][0] = fmaf(blk[m][0], fa, acc[m][0]);
+              acc[m][1] = fmaf(blk[m][1], fa, acc[m][1]);
+              acc[m][2] = fmaf(blk[m][2], fb, acc[m][2]);
+              acc[m][3] = fmaf(blk[m][3], fb, acc[m][3]);
+            }
+          }
+        } else if constexpr (FMT == FMT_INT8) {
+#pragma unroll
+          for (int pc = 0; pc < 8; ++pc) {
+            const uint32_t qa = q[pc >> 1][2 * (pc & 1)], qb = q[pc >> 1][2 * (pc & 1) + 1];
+            uint32_t a0, a1, a2, a3;
+            s8x4_to_f16x2x2(qa, a0, a2);
+            s8x4_to_f16x2x2(qb, a1, a3);
+            const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(g + 8 * m, (kx & 63) * 2));
+              mma_f16_16816(ui[pc & 1][m], a0, a1, a2, a3, xv.x, xv.y);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {  // 64-K halves of the chunk: the FP8 fold granularity
+            float blk[2][MT][4];            // two chains so consecutive MMAs are independent
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+              for (int m = 0; m < MT; ++m) blk[e][m][0] = blk[e][m][1] = blk[e][m][2] = blk[e][m][3] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int pc = 4 * hb + j;
+              const uint32_t qa = q[pc >> 1][2 * (pc & 1)], qb = q[pc >> 1][2 * (pc & 1) + 1];
+              const uint32_t a0 = e4m3x2_to_f16x2((uint16_t)(qa & 0xFFFFu));
+              const uint32_t a2 = e4m3x2_to_f16x2((uint16_t)(qa >> 16));
+              const uint32_t a1 = e4m3x2_to_f16x2((uint16_t)(qb & 0xFFFFu));
+              const uint32_t a3 = e4m3x2_to_f16x2((uint16_t)(qb >> 16));
+              const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
+#pragma unroll
+              for (int m = 0; m < MT; ++m) {
+                const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(g + 8 * m, (kx & 63) * 2));
+                mma_f16_16816(blk[j & 1][m], a0, a1, a2, a3, xv.x, xv.y);
+              }
+            }
+            const int k0 = (kt * S2_CHUNKS + ck) * 128 + 64 * hb;  // first K of this half
+            // block_k is a power of two; K past the last block (zero weights) has no scale byte
+            const float f = k0 < a.K ? ue8m0_to_f32(sc_row[min(k0, a.K - 1) >> a.bk_shift]) : 0.f;
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) acc[m][r] = fmaf(blk[0][m][r] + blk[1][m][r], f, acc[m][r]);
+          }
+        }
+      }
+      if constexpr (FMT == FMT_INT8) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acci[m][r] += __float2int_rn(ui[0][m][r] + ui[1][m][r]);
+      }
+      // every shared-memory fragment of the unit has been read: hand the stage back
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[slot]);
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    left -= seg_units;
+
+    // ------------------------------------------------------------ row-block (segment) end
+    float res[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) res[m][r] = kInt ? __int_as_float(acci[m][r]) : acc[m][r];
+    const int kt_end = kt;
+    const int seg_rb = rb;
+    rb += 1;  // the next segment (if any) starts a new row block
+    kt = 0;
+    if (kt0 == 0 && kt_end == nk) {
+      emit(seg_rb, res);
+      continue;
+    }
+    const int cf = s2_cta_of((int64_t)seg_rb * nk, T, G);
+    if (c == cf) {
+      // this CTA settles the block after its last unit (this is its last segment)
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) own[m][r] = res[m][r];
+      settle_rb = seg_rb;
+      continue;
+    }
+    // another CTA settles it: store the partial sums in this CTA's slot (a CTA posts at most
+    // once: for its first segment), then count in with release order
+    float* pb = a.part + (int64_t)c * 16 * S2_ROWS;
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int col = 2 * t + (r & 1) + 8 * m;
+        const int rl = 16 * w + g + (r >= 2 ? 8 : 0);
+        pb[col * S2_ROWS + rl] = res[m][r];
+      }
+    __threadfence();
+    consumer_sync();
+    if (threadIdx.x == 0) atomicAdd(&a.tickets[seg_rb], 1u);
+  }
+
+  // -------------------------------------------------------------- settle the shared block
+  if (settle_rb >= 0) {
+    const int grb = settle_rb;
+    const int cl = s2_cta_of((int64_t)grb * nk + nk - 1, T, G);
+    const int count = cl - c + 1;
+    // the other CTAs' partial sums: wait (bounded) until all count-1 of them are in
+    if (threadIdx.x == 0) {
+      uint32_t n = 0;
+      while (true) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(a.tickets + grb) : "memory");
+        if (v >= (unsigned)(count - 1)) break;
+        if (++n > lim || *abort) {
+          fail();
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    consumer_sync();
+    // this CTA's sums first, then CTAs c+1..cl in order, four slots' loads in flight at a time
+    float sum[MT][4];
+    int32_t sumi[MT][4];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        sum[m][r] = own[m][r];
+        sumi[m][r] = __float_as_int(own[m][r]);
+      }
+    for (int u0 = 1; u0 < count; u0 += 4) {
+      float v[MT][4][4];
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int col = 2 * t + (r & 1) + 8 * m;
+          const int rl = 16 * w + g + (r >= 2 ? 8 : 0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            v[m][r][k] = (u0 + k < count) ? __ldcg(a.part + ((int64_t)(c + u0 + k) * 16 + col) * S2_ROWS + rl) : 0.f;
+        }
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            if (u0 + k >= count) break;
+            if (kInt)
+              sumi[m][r] += __float_as_int(v[m][r][k]);
+            else
+              sum[m][r] += v[m][r][k];
+          }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) sum[m][r] = kInt ? __int_as_float(sumi[m][r]) : sum[m][r];
+    emit(grb, sum);
+    if (threadIdx.x == 0) a.tickets[grb] = 0;  // ready for the next call
+  }
+}
+
+}  // namespace ql

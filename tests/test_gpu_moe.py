@@ -87,6 +87,27 @@ def test_moe_small(ql, M):
     check_moe(c, run_moe(ql, c, wdev, topk), I, topk)
 
 
+@pytest.mark.parametrize("M,E,topk", [(1, 16, 4), (3, 16, 4), (9, 16, 4), (16, 16, 4), (16, 4, 2), (8, 64, 8)])
+def test_moe_small_persistent_kernel(ql, M, E, topk):
+    # H and I whole 256-K units: both expert GEMVs run on the persistent TMA kernel; (16, 4, 2)
+    # puts 8 pairs on each expert on average (up to all 16 tokens on one)
+    H, I = 512, 256
+    c = synth.moe_case(M, E, H, I, seed=40 + M + E)
+    wdev = [torch.from_numpy(c[k]).cuda() for k in ("w13", "s13", "w2", "s2")]
+    check_moe(c, run_moe(ql, c, wdev, topk), I, topk)
+
+
+def test_moe_persistent_given_ids(ql):
+    E, H, I, topk = 8, 256, 512, 2
+    c = synth.moe_case(4, E, H, I, seed=33)
+    wdev = [torch.from_numpy(c[k]).cuda() for k in ("w13", "s13", "w2", "s2")]
+    ids = np.array([[0, 7], [7, 0], [3, 4], [5, 6]], np.int32)
+    wts = np.array([[0.25, 0.75], [1.0, 0.5], [0.1, 0.2], [0.3, 0.3]], np.float32)
+    got = run_moe(ql, c, wdev, topk, ids=ids, wts=wts)
+    assert np.array_equal(got[1], ids)
+    check_moe(c, got, I, topk, ids=ids, wts=wts)
+
+
 def test_moe_given_ids_and_renormalised_routing(ql):
     E, H, I, topk = 8, 128, 128, 2
     c = synth.moe_case(4, E, H, I, seed=31)
