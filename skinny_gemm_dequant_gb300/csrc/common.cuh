@@ -90,6 +90,14 @@ __device__ __forceinline__ float ue8m0_to_f32(uint32_t b) {
   return __uint_as_float(b << 23);
 }
 
+// two UE8M0 bytes (low byte -> .x) to exact fp32 2^(b-127) (b = 0: 2^-127, b = 255: NaN) through
+// the hardware's ue8m0x2 -> bf16x2 conversion: bf16 keeps fp32's exponent range, so both are exact
+__device__ __forceinline__ float2 ue8m0x2_to_f32x2(uint32_t two_bytes) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.ue8m0x2 %0, %1;" : "=r"(r) : "h"((uint16_t)two_bytes));
+  return make_float2(__uint_as_float(r << 16), __uint_as_float(r & 0xFFFF0000u));
+}
+
 // ------------------------------------------------------------------ warp MMA (f16 -> f32)
 // D[16x8] += A[16x16] * B[16x8]; A row-major fragments a0..a3, B "col" fragments b0,b1.
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,

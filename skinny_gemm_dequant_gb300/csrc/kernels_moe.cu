@@ -4,8 +4,8 @@
 // p = softmax(logits) (evaluated in fp64, so the probabilities match an fp64 reference to the
 // last fp32 bit), the topk experts with the largest logits (equal logits: lower expert id
 // first), weights p[ids] (renormalised on request).  Dispatch groups the (token, slot) pairs
-// by expert with a stable counting sort and lists the distinct experts in first-use order;
-// the expert GEMMs launch one CTA column per distinct expert.
+// by expert (increasing id, stable in pair order) and lists the distinct experts in increasing
+// id; the expert GEMMs work on one slot per distinct expert.
 #include <atomic>
 
 #include "internal.h"
@@ -34,8 +34,10 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const MoeRoute
         mx = fmaxf(mx, v);
       }
       mx = warp_max(mx);
+      // exp in fp32 (within 2 ulp), summed in fp64: the probabilities stay within a few 1e-7
+      // of the fp64 softmax; the ids depend only on the (exact) logit comparisons
       double sum = 0.0;
-      for (int e = lane; e < E; e += 32) sum += exp((double)s_lg[m * E + e] - (double)mx);
+      for (int e = lane; e < E; e += 32) sum += (double)expf(s_lg[m * E + e] - mx);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       double wsum = 0.0;
@@ -57,7 +59,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const MoeRoute
         __syncwarp();
         if (lane == 0) taken[m * E + be] = 1;
         __syncwarp();
-        const double p = exp((double)bv - (double)mx) / sum;
+        const double p = (double)expf(bv - mx) / sum;
         pw[j] = p;
         wsum += p;
         if (lane == 0) {
@@ -90,25 +92,48 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const MoeRoute
   }
   for (int e = threadIdx.x; e <= E; e += blockDim.x) s_cnt[e] = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // stable counting sort of the pairs by expert; distinct experts in first-use order
-    for (int p = 0; p < P; ++p)
-      if (s_ids[p] >= 0) s_cnt[s_ids[p]]++;
-    int run = 0, nu = 0;
-    for (int e = 0; e < E; ++e) {
-      const int c = s_cnt[e];
+  // dispatch: pairs grouped by expert (increasing id), stable in pair order; distinct experts
+  // listed in increasing id
+  for (int p = threadIdx.x; p < P; p += blockDim.x)
+    if (s_ids[p] >= 0) atomicAdd(&s_cnt[s_ids[p]], 1);
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scans of the counts (offsets) and of the used flags (slots), E/32 per lane
+    const int per = (E + 31) / 32, e0 = lane * per;
+    int c = 0, u = 0;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      c += s_cnt[e];
+      u += s_cnt[e] > 0;
+    }
+    int ci = c, ui = u;  // inclusive warp scans
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int cv = __shfl_up_sync(0xffffffffu, ci, o), uv = __shfl_up_sync(0xffffffffu, ui, o);
+      if (lane >= o) {
+        ci += cv;
+        ui += uv;
+      }
+    }
+    int run = ci - c, nu = ui - u;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      const int n = s_cnt[e];
       r.offsets[e] = run;
-      s_cnt[e] = run;
-      run += c;
+      if (n > 0) r.uniq[nu++] = e;
+      s_cnt[e] = run;  // now the expert's first dispatch position
+      run += n;
     }
-    r.offsets[E] = run;
-    for (int p = 0; p < P; ++p) {
-      const int e = s_ids[p];
-      if (e < 0) continue;
-      if (r.offsets[e] == s_cnt[e]) r.uniq[nu++] = e;  // first pair of this expert
-      r.pairs[s_cnt[e]++] = p;
+    if (lane == 31) {
+      r.offsets[E] = run;
+      *r.nuniq = nu;
     }
-    *r.nuniq = nu;
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int e = s_ids[p];
+    if (e < 0) continue;
+    int rank = 0;  // earlier pairs of the same expert
+    for (int q = 0; q < p; ++q) rank += s_ids[q] == e;
+    r.pairs[s_cnt[e] + rank] = p;
   }
   __syncthreads();
   pdl_launch_dependents();

@@ -58,7 +58,7 @@ struct SkinnyArgs {
   // MoE
   const int32_t* offsets;   // [E+1]
   const int32_t* pairs;     // [M*topk] sorted by expert
-  const int32_t* uniq;      // [E] unique expert ids in first-use order
+  const int32_t* uniq;      // [E] distinct expert ids, increasing
   const int32_t* nuniq;     // [1]
   int topk, I;
   uint16_t* h;              // gate_up result [M*topk, I]

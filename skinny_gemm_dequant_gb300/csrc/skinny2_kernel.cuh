@@ -379,8 +379,12 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
               for (int m = 0; m < MT; ++m)
                 mma_f16_16816(blk[m], a0, a1, a2, a3, h ? xv[m].z : xv[m].x, h ? xv[m].w : xv[m].y);
             }
-            const float fa = ue8m0_to_f32((pc < 4 ? sa8.x : sa8.y) >> (8 * (pc & 3)));
-            const float fb = ue8m0_to_f32((pc < 4 ? sb8.x : sb8.y) >> (8 * (pc & 3)));
+            // the group's scale bytes of rows g (byte 0) and g+8 (byte 1), decoded together
+            uint32_t two;
+            asm("prmt.b32 %0, %1, %2, %3;" : "=r"(two) : "r"(pc < 4 ? sa8.x : sa8.y), "r"(pc < 4 ? sb8.x : sb8.y),
+                "r"((uint32_t)(((4 + (pc & 3)) << 4) | (pc & 3))));
+            const float2 fab = ue8m0x2_to_f32x2(two);
+            const float fa = fab.x, fb = fab.y;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
               acc[m][0] = fmaf(blk[m][0], fa, acc[m][0]);
