@@ -98,7 +98,7 @@ Dense2Layout dense2_layout(int fmt, int64_t Mc, int64_t N, int64_t K, int block_
 struct Moe2Layout {
   Skinny2Plan gu, dn;
   int slots, slot_rows;
-  size_t ids, wts, offsets, pairs, uniq, nuniq, gus, o, x16, tokf, part, total;
+  size_t ids, wts, offsets, pairs, rows, uniq, nuniq, gus, o, x16, tokf, part, total;
 };
 
 Moe2Layout moe2_layout(int64_t M, int64_t H, int64_t I, int E, int topk) {
@@ -113,6 +113,7 @@ Moe2Layout moe2_layout(int64_t M, int64_t H, int64_t I, int E, int topk) {
   l.wts = c.take(P * 4);
   l.offsets = c.take((E + 1) * 4);
   l.pairs = c.take(P * 4);
+  l.rows = c.take(P * 4);
   l.uniq = c.take((size_t)E * 4);
   l.nuniq = c.take(4);
   l.gus = c.take((size_t)P * 2 * I * 4);
@@ -547,25 +548,7 @@ ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint1
   if (moe2_ok(H, I, s13, s2)) {
     const Moe2Layout l = moe2_layout(M, H, I, E, topk);
     if ((int64_t)l.slots * (l.gu.nb > l.dn.nb ? l.gu.nb : l.dn.nb) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
-    MoeRouteArgs r = {};
-    r.logits = router_logits;
-    r.ids_in = topk_ids_in;
-    r.w_in = topk_w_in;
-    r.M = (int)M;
-    r.E = E;
-    r.topk = topk;
-    r.renorm = renormalize;
-    r.ids = at<int32_t>(workspace, l.ids);
-    r.wts = at<float>(workspace, l.wts);
-    r.offsets = at<int32_t>(workspace, l.offsets);
-    r.pairs = at<int32_t>(workspace, l.pairs);
-    r.uniq = at<int32_t>(workspace, l.uniq);
-    r.nuniq = at<int32_t>(workspace, l.nuniq);
-    r.ids_dbg = topk_ids_out;
-    r.w_dbg = topk_w_out;
-    r.status = at<uint32_t>(workspace, 0);
-    cudaError_t e = launch_moe_route(r, st);
-    if (e != cudaSuccess) return cuda_status(e);
+    cudaError_t e;
     Skinny2Args a = {};
     a.x16 = at<uint16_t>(workspace, l.x16);
     a.tokf = at<float>(workspace, l.tokf);
@@ -575,11 +558,20 @@ ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint1
     a.tickets = at<unsigned>(workspace, kTicketOff);
     a.status = at<uint32_t>(workspace, 0);
     a.wait_limit = g_wait_limit;
-    a.nuniq = r.nuniq;
-    a.uniq = r.uniq;
-    a.offsets = r.offsets;
-    a.pairs = r.pairs;
-    a.ids = r.ids;
+    // routing: done by the gate_up launch (CTA 0 writes the results for down and the combine)
+    a.logits = router_logits;
+    a.ids_in = topk_ids_in;
+    a.w_in = topk_w_in;
+    a.renorm = renormalize;
+    a.ids_dbg = topk_ids_out;
+    a.w_dbg = topk_w_out;
+    a.wts = at<float>(workspace, l.wts);
+    a.nuniq = at<int32_t>(workspace, l.nuniq);
+    a.uniq = at<int32_t>(workspace, l.uniq);
+    a.offsets = at<int32_t>(workspace, l.offsets);
+    a.pairs = at<int32_t>(workspace, l.pairs);
+    a.rows = at<int32_t>(workspace, l.rows);
+    a.ids = at<int32_t>(workspace, l.ids);
     a.topk = topk;
     a.E = E;
     a.I = (int)I;
@@ -609,7 +601,7 @@ ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint1
     a.o = at<float>(workspace, l.o);
     e = launch_moe2(S2_MOE_DN, l.dn, a, w2, I / 2, H * (I / 2), E, st);
     if (e != cudaSuccess) return cuda_status(e);
-    e = launch_moe_combine(a.o, r.ids, r.wts, (int)M, topk, (int)H, y, st);
+    e = launch_moe_combine(a.o, a.ids, a.wts, (int)M, topk, (int)H, y, st);
     if (e != cudaSuccess) return cuda_status(e);
     if (path_out) *path_out = QL_PATH_MOE_MXFP4;
     return QL_OK;

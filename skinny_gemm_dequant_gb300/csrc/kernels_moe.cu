@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const MoeRoute
       for (int e = lane; e < E; e += 32) sum += (double)expf(s_lg[m * E + e] - mx);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      const double rsum = 1.0 / sum;  // one fp64 division per token (fp64 is slow here)
       double wsum = 0.0;
       double pw[16];
       for (int j = 0; j < topk; ++j) {
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const MoeRoute
         __syncwarp();
         if (lane == 0) taken[m * E + be] = 1;
         __syncwarp();
-        const double p = (double)expf(bv - mx) / sum;
+        const double p = (double)expf(bv - mx) * rsum;
         pw[j] = p;
         wsum += p;
         if (lane == 0) {
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const MoeRoute
       }
       if (lane == 0) {
         for (int j = 0; j < topk; ++j) {
-          const float w = (float)(r.renorm ? pw[j] / wsum : pw[j]);
+          const float w = (float)(r.renorm ? pw[j] * (1.0 / wsum) : pw[j]);
           r.wts[m * topk + j] = w;
           if (r.w_dbg) r.w_dbg[m * topk + j] = w;
           if (r.ids_dbg) r.ids_dbg[m * topk + j] = s_ids[m * topk + j];

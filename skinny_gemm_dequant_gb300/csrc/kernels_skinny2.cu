@@ -87,7 +87,9 @@ static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w
   using Tr = S2Traits<FMT>;
   constexpr uint32_t STAGE = s2_stage_bytes<FMT, MT>();
   constexpr int Mp = 8 * MT;
-  const size_t fixed = 1024 + p.fp8_scale_bytes + 256;  // alignment slack, FP8 scale rows, static
+  // behind the ring: FP8 block-scale rows (dense FP8) or the routing (MoE gate_up)
+  const size_t extra = p.fp8_scale_bytes + (KIND == S2_MOE_GU ? s2_route_bytes(a.M * a.topk, a.E) : 0);
+  const size_t fixed = 1024 + extra + 256;  // alignment slack, extra, static
   // per CTA: the SM's 228 KB less 1 KB reserved per resident CTA, capped by the opt-in limit
   const int optin = s2_ctas_per_sm(MT) == 1 ? 227 * 1024 : (228 * 1024) / s2_ctas_per_sm(MT) - 1024;
   int S = (int)((optin - fixed) / (STAGE + 16));
@@ -101,7 +103,7 @@ static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w
   a.total = p.total;
   const uint64_t wbytes = FMT == FMT_MXFP4 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
   a.wbytes = (int)wbytes;
-  const size_t smem = 1024 + (size_t)S * STAGE + (size_t)S * 16 + p.fp8_scale_bytes;
+  const size_t smem = 1024 + (size_t)S * STAGE + (size_t)S * 16 + extra;
   CUtensorMap tw, tw2, tx;
   // whole 128-byte chunks as the third dimension (a box of 2 chunks is one 32 KB TMA operation),
   // experts as the fourth

@@ -75,12 +75,22 @@ struct Skinny2Args {
   int32_t* acc_out;
   float* part;        // [CTAs][16][128] partial sums (fp32 or int32 bits): each CTA posts at most one
   unsigned* tickets;  // [row blocks] arrival counts of the partial sums
-  // MoE (routing results of the router kernel; experts in distinct-expert slots)
-  const int32_t* nuniq;    // distinct experts
-  const int32_t* uniq;     // [slots] expert of each slot
-  const int32_t* offsets;  // [E+1] dispatch positions of each expert's (token, slot) pairs
-  const int32_t* pairs;    // [pairs] pair index m*topk+j at each dispatch position
-  const int32_t* ids;      // [M*topk] expert of each pair (-1: none)
+  // MoE routing: the gate_up launch routes (every CTA, identically) and its CTA 0 writes the
+  // results below, which the down launch and the combine read; experts sit in distinct-expert
+  // slots in increasing id
+  const uint16_t* logits;  // bf16 [M, E] router logits, or null with ids_in / w_in given
+  const int32_t* ids_in;   // [M*topk] given expert ids
+  const float* w_in;       // [M*topk] given routing weights
+  int renorm;              // renormalise the top-k probabilities to sum 1
+  int32_t* ids_dbg;        // optional copies of ids / weights
+  float* w_dbg;
+  float* wts;              // [M*topk] routing weights
+  int32_t* nuniq;          // distinct experts
+  int32_t* uniq;           // [slots] expert of each slot
+  int32_t* offsets;        // [E+1] dispatch positions of each expert's (token, slot) pairs
+  int32_t* pairs;          // [pairs] pair index m*topk+j at each dispatch position
+  int32_t* ids;            // [M*topk] expert of each pair (-1: none)
+  int32_t* rows;           // [pairs] down-stage image row of each dispatch position (-1: none)
   int topk, E;
   int slot_rows;           // MoE down: image rows per expert slot (8*MT)
   int64_t s_estride;       // MXFP4 scale bytes per expert
@@ -276,24 +286,13 @@ __device__ void s2_prepare(const Skinny2Args& a, int m, int sl, int nsl, int tid
 // at position q went to expert e; its gate and up sums g, u (length I) are gu[p].  Its activation
 // row is h = bf16(silu(g) * u) (the expert's intermediate, rounded to bf16 as the pages' BF16
 // experts do), written as an f16 image row h * 2^-p (p from the row's amax, as for bf16 inputs)
-// at row slot(e) * slot_rows + (q - offsets[e]) of every copy; slice 0 writes 2^p for the
-// epilogue.  A pair beyond slot_rows of its expert (only possible when a token lists an expert
+// at row rows[q] = slot(e) * slot_rows + (q - offsets[e]) of every copy (the routing wrote it);
+// slice 0 writes 2^p for the epilogue.  A pair beyond slot_rows of its expert (only possible when a token lists an expert
 // twice) gets no row.
-__device__ inline void s2_prepare_h(const Skinny2Args& a, int q, int sl, int nsl, int nu, int tid, float* red) {
+__device__ inline void s2_prepare_h(const Skinny2Args& a, int q, int sl, int nsl, int tid, float* red) {
   const int p = a.pairs[q];
-  int lo = 0, hi = a.E - 1;  // the expert of position q: the largest e with offsets[e] <= q
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (a.offsets[mid] <= q)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  const int e = lo, j = q - a.offsets[e];
-  int u = 0;
-  while (u < nu - 1 && a.uniq[u] != e) ++u;
-  const bool has_row = j < a.slot_rows;
-  const int r = u * a.slot_rows + j;
+  const int r = a.rows[q];  // slot(e) * slot_rows + rank within the expert's pairs, or -1
+  const bool has_row = r >= 0;
   const int I = a.I, nvec = I / 8;
   const float* gp = a.gu + (int64_t)p * 2 * I;
   auto hvals = [&](int i, float (&h)[8], uint16_t (&hb)[8]) {
@@ -350,6 +349,156 @@ __device__ inline void s2_prepare_h(const Skinny2Args& a, int q, int sl, int nsl
       for (int cp = 0; cp < a.xcopies; ++cp) *reinterpret_cast<uint4*>(out + cp * cstride + 8 * i) = make_uint4(0, 0, 0, 0);
   if (has_row && sl == 0 && tid == 0) a.tokf[r] = __uint_as_float((uint32_t)(127 + pe) << 23);
   consumer_sync();  // red[] is reused by the next job
+}
+
+// MoE routing inside the gate_up launch (softmax top-k, [DSV4] routing and grouped dispatch):
+// per token p = softmax(logits) (fp32 exponentials within 2 ulp, summed in fp64), the topk
+// experts with the largest logits (equal logits: lower id first) and weights p[ids]
+// (renormalised on request); or the given ids and weights.  Then the pairs are grouped by expert
+// (increasing id, stable in pair order) and the distinct experts listed in increasing id.  Every
+// CTA computes the same routing into its shared memory (ids, first dispatch position per
+// expert, distinct experts, their count); CTA 0 also writes it all out.  All threads of the CTA
+// call this (E <= 1024, M*topk <= 256).
+__device__ inline void s2_route(const Skinny2Args& a, int* s_ids, double* s_pw, int* s_cnt, int* s_uniq, int* s_slot,
+                                int* s_nu) {
+  const int M = a.M, E = a.E, topk = a.topk, P = M * topk;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const bool out = blockIdx.x == 0;
+  if (a.logits) {
+    for (int m = warp; m < M; m += nw) {  // a warp per token, the logits in registers
+      float lv[32];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int e = lane + 32 * j;
+        lv[j] = e < E ? bf16_bits_to_f32(a.logits[(int64_t)m * E + e]) : -INFINITY;
+        mx = fmaxf(mx, lv[j]);
+      }
+      mx = warp_max(mx);
+      double sum = 0.0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (lane + 32 * j < E) sum += (double)expf(lv[j] - mx);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      // one fp64 division per token (fp64 is slow on this part): p = e * (1/sum) is within one
+      // fp64 ulp of e / sum, far below the fp32 weights' precision
+      const double rsum = 1.0 / sum;
+      uint32_t taken = 0;
+      double wsum = 0.0;
+      for (int k = 0; k < topk; ++k) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int e = lane + 32 * j;
+          if (e < E && !((taken >> j) & 1u) && (lv[j] > bv || (lv[j] == bv && e < be))) {
+            bv = lv[j];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (ov > bv || (ov == bv && oe < be)) {
+            bv = ov;
+            be = oe;
+          }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        const double pr = (double)expf(bv - mx) * rsum;
+        wsum += pr;
+        if (lane == 0) {
+          s_ids[m * topk + k] = be;
+          s_pw[m * topk + k] = pr;
+        }
+      }
+      __syncwarp();
+      if (out && lane < topk) {
+        const int pi = m * topk + lane;
+        const float w = (float)(a.renorm ? s_pw[pi] * (1.0 / wsum) : s_pw[pi]);
+        a.ids[pi] = s_ids[pi];
+        a.wts[pi] = w;
+        if (a.ids_dbg) a.ids_dbg[pi] = s_ids[pi];
+        if (a.w_dbg) a.w_dbg[pi] = w;
+      }
+    }
+  } else {
+    for (int pi = threadIdx.x; pi < P; pi += blockDim.x) {
+      int e = a.ids_in[pi];
+      if (e < 0 || e >= E) {
+        if (out) raise_flag(a.status, 2u);
+        e = -1;
+      }
+      s_ids[pi] = e;
+      if (out) {
+        a.ids[pi] = e;
+        a.wts[pi] = a.w_in[pi];
+        if (a.ids_dbg) a.ids_dbg[pi] = e;
+        if (a.w_dbg) a.w_dbg[pi] = a.w_in[pi];
+      }
+    }
+  }
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) s_cnt[e] = 0;
+  __syncthreads();
+  for (int pi = threadIdx.x; pi < P; pi += blockDim.x)
+    if (s_ids[pi] >= 0) atomicAdd(&s_cnt[s_ids[pi]], 1);
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scans of the counts (dispatch offsets) and of the used flags (slots)
+    const int per = (E + 31) / 32, e0 = lane * per;
+    int c = 0, u = 0;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      c += s_cnt[e];
+      u += s_cnt[e] > 0;
+    }
+    int ci = c, ui = u;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int cv = __shfl_up_sync(0xffffffffu, ci, o), uv = __shfl_up_sync(0xffffffffu, ui, o);
+      if (lane >= o) {
+        ci += cv;
+        ui += uv;
+      }
+    }
+    int run = ci - c, nu = ui - u;
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      const int n = s_cnt[e];
+      if (out) a.offsets[e] = run;
+      if (n > 0) {
+        s_uniq[nu] = e;
+        if (out) a.uniq[nu] = e;
+        ++nu;
+      }
+      s_cnt[e] = run;                   // now the expert's first dispatch position
+      s_slot[e] = n > 0 ? nu - 1 : -1;  // and its slot
+      run += n;
+    }
+    if (lane == 31) {
+      *s_nu = nu;
+      if (out) {
+        a.offsets[E] = run;
+        *a.nuniq = nu;
+      }
+    }
+  }
+  __syncthreads();
+  if (out)
+    for (int pi = threadIdx.x; pi < P; pi += blockDim.x) {
+      const int e = s_ids[pi];
+      if (e < 0) continue;
+      int rank = 0;  // earlier pairs of the same expert
+      for (int q = 0; q < pi; ++q) rank += s_ids[q] == e;
+      a.pairs[s_cnt[e] + rank] = pi;
+      a.rows[s_cnt[e] + rank] = rank < a.slot_rows ? s_slot[e] * a.slot_rows + rank : -1;
+    }
+}
+
+// shared memory of s2_route: weights [P] double, ids [P] int, counts [E+1] int, slot experts [E]
+// int, slot of each expert [E] int, count
+__host__ __device__ inline size_t s2_route_bytes(int P, int E) {
+  return ((size_t)P * 8 + (size_t)P * 4 + (size_t)(3 * E + 2) * 4 + 15) & ~size_t(15);
 }
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, int x, int y, int z, int w,

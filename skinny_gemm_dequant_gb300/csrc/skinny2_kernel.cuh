@@ -2,7 +2,7 @@
 //
 // One kernel serves three kinds of launch:
 //  * S2_DENSE: y = dequant(W) x for INT8 / FP8-block / MXFP4 weights (M <= 16 tokens);
-//  * S2_MOE_GU: MoE stage 1, for every distinct routed expert e the gate and up rows of W13[e]
+//  * S2_MOE_GU: MoE stage 1 (routing included), for every distinct routed expert e the gate and up rows of W13[e]
 //    against all M tokens' activations (the MMA's 8 or 16 token columns cost the same however
 //    many are routed); the epilogue keeps the (token, e) pairs the router chose and stores their
 //    raw sums gu[pair] in fp32;
@@ -48,11 +48,28 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, c = blockIdx.x;
-  // MoE: the units follow the router's distinct experts (the kernel before this one)
+  // MoE: the units follow the distinct routed experts.  gate_up routes here (every CTA alike,
+  // into shared memory behind the ring); down reads what gate_up's CTA 0 wrote.
   int nu = 1;
+  const int32_t* r_uniq = a.uniq;  // expert of each slot
+  const int32_t* r_ids = a.ids;    // expert of each pair
   if constexpr (kMoE) {
     pdl_wait();
-    nu = min(*a.nuniq, a.E);
+    if constexpr (KIND == S2_MOE_GU) {
+      const int P = a.M * a.topk;
+      double* s_pw = reinterpret_cast<double*>(fp8sc);  // no FP8 scale rows for MXFP4
+      int* s_ids = reinterpret_cast<int*>(s_pw + P);
+      int* s_cnt = s_ids + P;
+      int* s_uniq = s_cnt + a.E + 1;
+      int* s_slot = s_uniq + a.E;
+      int* s_nu = s_slot + a.E;
+      s2_route(a, s_ids, s_pw, s_cnt, s_uniq, s_slot, s_nu);
+      nu = *s_nu;
+      r_uniq = s_uniq;
+      r_ids = s_ids;
+    } else {
+      nu = min(*a.nuniq, a.E);
+    }
   }
   const int64_t T = kMoE ? (int64_t)nu * a.nb * a.nk : a.total;
   const int64_t s0 = (int64_t)c * T / G, s1 = (int64_t)(c + 1) * T / G;
@@ -125,7 +142,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
     // unit counters kept incrementally: no divisions in the loop
     int rb = rb_first, kt = (int)(s0 - (int64_t)rb_first * nk);
     int u = kMoE ? rb / a.nb : 0, rbl = rb - u * a.nb;  // expert slot, block within the expert
-    int ex = kMoE ? a.uniq[u] : 0;                      // expert
+    int ex = kMoE ? r_uniq[u] : 0;                      // expert
     int slot = 0;
     uint32_t phase = 0;  // (i / S) & 1
     for (int i = 0; i < n_units; ++i) {
@@ -191,7 +208,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
         if (++rbl == a.nb) {
           rbl = 0;
           ++u;
-          if (kMoE && u < nu) ex = a.uniq[u];
+          if (kMoE && u < nu) ex = r_uniq[u];
         }
       }
       if (++slot == S) {
@@ -216,7 +233,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
     unsigned mine = 0;
     for (int j = c; j < njob_rows * nsl; j += G, ++mine) {
       if constexpr (KIND == S2_MOE_DN)
-        s2_prepare_h(a, j % njob_rows, j / njob_rows, nsl, nu, threadIdx.x, s_red);
+        s2_prepare_h(a, j % njob_rows, j / njob_rows, nsl, threadIdx.x, s_red);
       else
         s2_prepare<FMT>(a, j % njob_rows, j / njob_rows, nsl, threadIdx.x, s_red);
     }
@@ -240,7 +257,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
   auto emit = [&](int grb, const float (&res)[MT][4]) {
     const int eu = kMoE ? grb / a.nb : 0;  // expert slot
     const int row_w = (grb - eu * a.nb) * S2_ROWS + 16 * w;
-    const int ex = kMoE ? a.uniq[eu] : 0;
+    const int ex = kMoE ? r_uniq[eu] : 0;
     int beg = 0, cnt = a.M;  // MoE down: the expert's pairs are dispatch positions beg..beg+cnt-1
     if constexpr (KIND == S2_MOE_DN) {
       beg = a.offsets[ex];
@@ -274,7 +291,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
           // keep the sums of the pair (token col, expert ex), if the router chose it
           int p = -1;
           for (int k = 0; k < a.topk; ++k)
-            if (a.ids[col * a.topk + k] == ex) p = col * a.topk + k;
+            if (r_ids[col * a.topk + k] == ex) p = col * a.topk + k;
           if (p >= 0) a.gu[(int64_t)p * a.N + row] = res[m][r] * colf[m][r & 1];
         } else if constexpr (KIND == S2_MOE_DN) {
           a.o[(int64_t)a.pairs[beg + col] * a.N + row] = res[m][r] * colf[m][r & 1];
