@@ -155,6 +155,25 @@ def fp8_block(x, w_codes, w_scale_bytes, K, block_n=128, block_k=128, a_scale=No
 
 
 # ----------------------------------------------------------------------------------------
+# BF16 dense decode GEMV ([Z100] §二.2.3, the bf16 route: bf16 values widen to fp32 exactly and
+# are multiplied and summed).  y[m, n] = sum_k x[m, k] w[n, k], both operands bf16.
+# ----------------------------------------------------------------------------------------
+
+
+def bf16_linear(x_bits, w_bits, K, rows=None):
+    """Unquantised linear on bf16 operands, exact in fp64.
+
+    x_bits: bf16 bits [M, K]; w_bits: bf16 bits [N, ldw] (only the first K columns are used:
+    padded rows allowed).  Returns (y fp64 [M, len(rows)], abs_sum fp64 [M, len(rows)]) with
+    abs_sum = sum_k |x w|, the error scale of the float tolerance."""
+    x = bf16_to_f64(np.asarray(x_bits)[:, :K])
+    w_bits = np.asarray(w_bits)
+    rows = np.arange(w_bits.shape[0]) if rows is None else np.asarray(rows)
+    w = bf16_to_f64(w_bits[rows, :K])
+    return x @ w.T, np.abs(x) @ np.abs(w).T
+
+
+# ----------------------------------------------------------------------------------------
 # 1x128 dynamic E4M3 activation quantisation with UE8M0 scales ([DSV4] §3.3 quant_config:
 # activation_scheme dynamic, fmt e4m3, scale_fmt ue8m0; [Z100] §二.2.4 a_s[m, kb]).
 # ----------------------------------------------------------------------------------------

@@ -70,6 +70,16 @@ def fp8_block_case(M, N, K, seed=0, ldw=None, block_n=128, block_k=128, s_lo=118
 
 
 # ---------------------------------------------------------------- MXFP4 cases
+def bf16_dense_case(M, N, K, seed=0, ldw=None):
+    """BF16 dense weights: w ~ N(0, 0.05^2) bf16 [N, ldw] (padding columns hold a NaN, so a
+    kernel that reads past K shows it), x ~ N(0,1) bf16 [M, K]."""
+    ldw = K if ldw is None else ldw
+    w = np.full((N, ldw), 0x7FC0, dtype=np.uint16)
+    w[:, :K] = f32_to_bf16_bits(0.05 * rng(seed, _W).standard_normal(size=(N, K), dtype=np.float32))
+    x = bf16_normal(rng(seed, _X), (M, K))
+    return {"x": x, "w": w}
+
+
 def mxfp4_dense_case(M, N, K, seed=0, s_lo=120, s_hi=127):
     """MXFP4 weights: uniform random E2M1 codes packed two per byte [N, K/2], UE8M0 per 32
     along K uniform in [s_lo, s_hi] [N, K/32]; x ~ N(0,1) bf16 [M, K]."""

@@ -183,3 +183,44 @@ def test_planted_transposed_scale_index_is_caught(monkeypatch):
     monkeypatch.setattr(Q, "fp8_block", transposed)
     with pytest.raises(AssertionError):
         test_fp8_block_scale_grid_orientation()
+
+
+# ------------------------------------------------------------------ BF16 dense GEMV
+def test_bf16_linear_exact_rational():
+    # every bf16 value is a dyadic rational: the oracle's fp64 sums of these small cases are
+    # exact, so they must equal the Fraction dot products
+    c = synth.bf16_dense_case(3, 5, 24, seed=3)
+    y, a = Q.bf16_linear(c["x"], c["w"], 24)
+    xv = F.bf16_to_f64(c["x"])
+    wv = F.bf16_to_f64(c["w"][:, :24])
+    for m in range(3):
+        for n in range(5):
+            ref = sum(Fraction(float(xv[m, k])) * Fraction(float(wv[n, k])) for k in range(24))
+            aref = sum(abs(Fraction(float(xv[m, k])) * Fraction(float(wv[n, k]))) for k in range(24))
+            assert Fraction(float(y[m, n])) == ref
+            assert Fraction(float(a[m, n])) == aref
+
+
+def test_bf16_linear_identity_and_padding():
+    # W = I picks the activations; NaN padding past K is never read
+    K = 16
+    x = synth.bf16_dense_case(2, 1, K, seed=4)["x"]
+    w = np.full((K, K + 8), 0x7FC0, np.uint16)
+    w[:, :K] = 0
+    w[np.arange(K), np.arange(K)] = 0x3F80  # bf16 1.0
+    y, a = Q.bf16_linear(x, w, K)
+    assert np.array_equal(y, F.bf16_to_f64(x))
+    assert np.array_equal(a, np.abs(F.bf16_to_f64(x)))
+
+
+def test_bf16_linear_row_subset_and_transpose():
+    # rows= selects output columns; a wrong operand orientation would break the shape or values
+    c = synth.bf16_dense_case(2, 7, 32, seed=5)
+    y, _ = Q.bf16_linear(c["x"], c["w"], 32)
+    ys, _ = Q.bf16_linear(c["x"], c["w"], 32, rows=[6, 1])
+    assert y.shape == (2, 7) and np.array_equal(ys, y[:, [6, 1]])
+    # a planted mistake (w used without the transpose on a square case) must not agree
+    sq = synth.bf16_dense_case(3, 3, 3, seed=6)
+    yy, _ = Q.bf16_linear(sq["x"], sq["w"], 3)
+    wrong = F.bf16_to_f64(sq["x"]) @ F.bf16_to_f64(sq["w"])
+    assert not np.allclose(yy, wrong)
