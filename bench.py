@@ -52,6 +52,10 @@ def bytes_fp8(M, N, K):
     return N * K + (-(-N // 128)) * (-(-K // 128)) + 2 * M * K + 2 * M * N
 
 
+def bytes_bf16(M, N, K):
+    return 2 * N * K + 2 * M * K + 2 * M * N
+
+
 def bytes_mxfp4(M, N, K):
     return N * K // 2 + N * K // 32 + 2 * M * K + 2 * M * N
 
@@ -290,12 +294,41 @@ def build_c4(ql, torch):
     return Workload("c4", calls, 2 * len(calls), cfg)
 
 
-BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4": build_c4}
+N4_MS = [1, 4, 16]
+
+
+def build_n4(ql, torch):
+    """BF16 dense decode GEMV (a NEXT row: unquantised weights on the same skinny kernel)."""
+    calls = []
+    weights = {}
+    for (N, K) in C2_SHAPES:
+        c = synth.bf16_dense_case(1, N, K, seed=0)
+        w0 = torch.from_numpy(c["w"].view(np.int16)).cuda().view(torch.bfloat16)
+        weights[(N, K)] = ([w0] + [w0.clone() for _ in range(ROTATE - 1)], {"i": 0})
+    for M in N4_MS:
+        for (N, K) in C2_SHAPES:
+            ws, state = weights[(N, K)]
+            x = dev_bf16(synth.bf16_dense_case(M, 1, K, seed=1)["x"], torch)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+
+            def call(ws=ws, x=x, y=y, state=state):
+                w = ws[state["i"] % ROTATE]
+                state["i"] += 1
+                ql.qlinear_bf16(x, w, out=y)
+
+            calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": bytes_bf16(M, N, K), "flops": 2 * M * N * K,
+                          "x": x, "y": y, "kind": "bf16"})
+    cfg = {"workload": "BF16 dense decode GEMV (unquantised weights), (N,K) in {(17408,5120),(5120,17408)} "
+                       "x M in {1,4,16}"}
+    return Workload("n4", calls, len(calls), cfg)
+
+
+BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4": build_c4, "n4": build_n4}
 
 _SKINNY = ("skinny2_kernel (one launch per call: activation preparation + weight-streaming GEMM); "
            "achieved = algorithmic bytes per call / CUDA-event time per call (graphs of 32 back-to-back "
            "calls), aggregated over the step's calls")
-KERNEL_DESC = {"c0": _SKINNY, "c1": _SKINNY, "c2": _SKINNY,
+KERNEL_DESC = {"c0": _SKINNY, "c1": _SKINNY, "c2": _SKINNY, "n4": _SKINNY,
                "c3": "MoE launches per call (routing, gate_up, down, combine); bytes of the touched experts / "
                      "event time per call",
                "c4": "tcgen05 block-scaled GEMM + its activation-quantisation launch; bytes / event time per call"}
@@ -431,6 +464,16 @@ def oracle_sample(config, rows_per_call):
             sec += time.perf_counter() - t
             done += len(np.unique(ids)) * 2 * len(cols) * (H // 2 + H // 32)
         desc = f"MoE oracle routing + gate_up on {rows_per_call} intermediate rows for M=1 and M=9"
+    elif config == "n4":
+        for (N, K) in C2_SHAPES:
+            c = _case(("bf16", N, K), lambda: synth.bf16_dense_case(16, N, K, seed=0))
+            rows = np.arange(min(rows_per_call, N))
+            for M in N4_MS:
+                t = time.perf_counter()
+                Q.bf16_linear(c["x"][:M], c["w"], K, rows=rows)
+                sec += time.perf_counter() - t
+                done += bytes_bf16(M, len(rows), K)
+        desc = f"BF16 oracle on the first {rows_per_call} output rows of each of the 6 calls"
     else:
         N, K = 17408, 5120
         c = _case(("fp8", N, K, 64), lambda: synth.fp8_block_case(64, N, K, seed=0))
@@ -536,7 +579,7 @@ def main():
 
     import torch
     if args.steps is None:
-        args.steps = {"c0": 20000, "c1": 4000, "c2": 4000, "c3": 2000, "c4": 2000}[args.config]
+        args.steps = {"c0": 20000, "c1": 4000, "c2": 4000, "c3": 2000, "c4": 2000, "n4": 2000}[args.config]
     torch.cuda.set_device(local)
     pg = None
     if ws > 1:
@@ -598,7 +641,8 @@ def main():
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": {"c0": "int8", "c1": "int8", "c2": "fp8", "c3": "fp4", "c4": "fp8/fp4"}[
+            "vs_baseline": None, "dtype": {"c0": "int8", "c1": "int8", "c2": "fp8", "c3": "fp4", "c4": "fp8/fp4",
+                                           "n4": "bf16"}[
                 args.config], "data": "synthetic",
             "config": dict(wl.cfg, parallelism=f"replicas x{ws}", l2="weights rotate over 6 copies per shape "
                                                                    "(inputs larger than L2)"),

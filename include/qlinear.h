@@ -56,7 +56,7 @@ typedef enum {
 } ql_status;
 
 /* operation ids for ql_workspace_bytes */
-enum { QL_OP_INT8_W8A8 = 1, QL_OP_FP8_BLOCK = 2, QL_OP_MXFP4 = 3, QL_OP_MOE_MXFP4 = 4 };
+enum { QL_OP_INT8_W8A8 = 1, QL_OP_FP8_BLOCK = 2, QL_OP_MXFP4 = 3, QL_OP_MOE_MXFP4 = 4, QL_OP_BF16 = 5 };
 
 /* activation modes of the FP8-block and MXFP4 linears */
 enum {
@@ -75,7 +75,8 @@ enum {
   QL_PATH_FP8_TCGEN05 = 3,     /* 1x128 act quant + tcgen05 block-scaled GEMM (FP8 x FP8)   */
   QL_PATH_MXFP4_SKINNY = 4,    /* MXFP4 skinny GEMM, bf16 activations                       */
   QL_PATH_MXFP4_TCGEN05 = 5,   /* 1x128 act quant + tcgen05 block-scaled GEMM (E4M3 x E2M1) */
-  QL_PATH_MOE_MXFP4 = 6        /* routing + dispatch + gate_up/SiLU + down + combine         */
+  QL_PATH_MOE_MXFP4 = 6,       /* routing + dispatch + gate_up/SiLU + down + combine         */
+  QL_PATH_BF16_SKINNY = 7      /* BF16 skinny GEMM (unquantised weights)                    */
 };
 
 /* device status flags (bitmask) */
@@ -172,6 +173,22 @@ QL_API ql_status qlinear_mxfp4(const uint16_t* x, int64_t M, int64_t K, int64_t 
                         uint8_t* aq_out, uint8_t* as_out,
                         void* workspace, size_t workspace_bytes, ql_stream_t stream,
                         int* path_out);
+
+/*
+ * BF16 dense decode GEMV, unquantised weights ([Z100] §二.2.3, the bf16 route: bf16 widened to
+ * fp32 exactly, products summed in fp32):
+ *   y[m,n] = bf16( sum_k x[m,k] * w[n,k] ) (+ bias, added after the cast and rounded again)
+ * x: bf16 [M, ldx] (device), w: bf16 [N, ldw] (device, K used, padded rows allowed), bias:
+ * bf16 [N] or null, y: bf16 [M, ldy] (device).  The caller owns every buffer; nothing is
+ * retained after the call returns.  Runs the persistent skinny kernel 16 tokens at a time.
+ * Requires K % 8 == 0, ldx % 8 == 0, ldw % 8 == 0, 16-byte aligned x and w, ldy >= N; returns
+ * QL_ERR_INVALID_ARG / QL_ERR_ALIGNMENT / QL_ERR_UNSUPPORTED before any launch otherwise.
+ * workspace: ql_workspace_bytes(QL_OP_BF16, M, N, K, 0, 0) bytes, zeroed once.
+ */
+QL_API ql_status qlinear_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                       const uint16_t* w, int64_t N, int64_t ldw, const uint16_t* bias,
+                       uint16_t* y, int64_t ldy, void* workspace, size_t workspace_bytes,
+                       ql_stream_t stream, int* path_out);
 
 /*
  * MXFP4 mixture-of-experts decode layer ([DSV4] §0.1 "M=1 MoE routing Q1", §0.3 grouped

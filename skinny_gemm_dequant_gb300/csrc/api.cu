@@ -288,6 +288,8 @@ size_t ql_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int to
       const size_t b = act_quant_ws(M, K);
       return a > b ? a : b;
     }
+    case QL_OP_BF16:
+      return dense2_layout(FMT_BF16, Mc, N, K, 128).total;
     case QL_OP_MOE_MXFP4: {
       if (E <= 0 || topk <= 0) return 0;
       const size_t a = moe_layout(M, N, K, E, topk).total, b = moe2_layout(M, N, K, E, topk).total;
@@ -457,6 +459,35 @@ ql_status qlinear_fp8_block(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
   if (e != cudaSuccess) return cuda_status(e);
   if (path_out) *path_out = QL_PATH_FP8_TCGEN05;
   return QL_OK;
+}
+
+// ------------------------------------------------------------------ BF16 dense
+ql_status qlinear_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const uint16_t* w, int64_t N,
+                       int64_t ldw, const uint16_t* bias, uint16_t* y, int64_t ldy, void* workspace,
+                       size_t workspace_bytes, ql_stream_t stream, int* path_out) {
+  if (path_out) *path_out = QL_PATH_NONE;
+  if (!x || !w || !y) return QL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldx < K || ldw < K || ldy < N) return QL_ERR_INVALID_ARG;
+  if (M > 65535 || N > (1 << 30) || K > (1 << 28)) return QL_ERR_UNSUPPORTED;
+  if (K % 8 != 0 || cdiv(N, S2_ROWS) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
+  if (!al16(x) || !al16(w) || ldx % 8 != 0 || ldw % 8 != 0) return QL_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < ql_workspace_bytes(QL_OP_BF16, M, N, K, 0, 0)) return QL_ERR_WORKSPACE;
+  if (!al16(workspace)) return QL_ERR_ALIGNMENT;
+  Dense2Call d = {};
+  d.fmt = FMT_BF16;
+  d.x = x;
+  d.M = M;
+  d.K = K;
+  d.ldx = ldx;
+  d.w = reinterpret_cast<const uint8_t*>(w);
+  d.N = N;
+  d.ldw = ldw * 2;  // bytes
+  d.bias = bias;
+  d.y = y;
+  d.ldy = ldy;
+  const ql_status s = run_dense2(d, workspace, (cudaStream_t)stream);
+  if (s == QL_OK && path_out) *path_out = QL_PATH_BF16_SKINNY;
+  return s;
 }
 
 // ------------------------------------------------------------------ MXFP4 dense

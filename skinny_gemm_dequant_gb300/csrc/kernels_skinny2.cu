@@ -18,7 +18,8 @@ Skinny2Plan skinny2_plan(int fmt, int64_t M, int64_t N, int64_t K, int block_n, 
   Skinny2Plan p;
   p.mt = M <= 8 ? 1 : 2;
   p.mp = 8 * p.mt;
-  const int kpu = fmt == FMT_MXFP4 ? S2Traits<FMT_MXFP4>::KPU : S2Traits<FMT_INT8>::KPU;  // K per unit
+  const int kpu = fmt == FMT_MXFP4 ? S2Traits<FMT_MXFP4>::KPU
+                                   : (fmt == FMT_BF16 ? S2Traits<FMT_BF16>::KPU : S2Traits<FMT_INT8>::KPU);  // K per unit
   p.nb = (N + S2_ROWS - 1) / S2_ROWS;
   p.nk = (int)((K + kpu - 1) / kpu);
   p.kpad = (int64_t)p.nk * kpu;
@@ -101,7 +102,7 @@ static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w
   a.nk = p.nk;
   a.nb = (int)p.nb;
   a.total = p.total;
-  const uint64_t wbytes = FMT == FMT_MXFP4 ? (uint64_t)a.K / 2 : (uint64_t)a.K;
+  const uint64_t wbytes = FMT == FMT_MXFP4 ? (uint64_t)a.K / 2 : (FMT == FMT_BF16 ? (uint64_t)a.K * 2 : (uint64_t)a.K);
   a.wbytes = (int)wbytes;
   const size_t smem = 1024 + (size_t)S * STAGE + (size_t)S * 16 + extra;
   CUtensorMap tw, tw2, tx;
@@ -118,7 +119,12 @@ static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w
     return cudaErrorInvalidValue;
   a.xcopies = kXCopies;
   a.kpad = p.kpad;
-  {
+  if (FMT == FMT_BF16) {
+    // the caller's x [M][ldx] bf16: boxes of 64 columns x Mp rows, zeros past K and past M
+    if (!map2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.ldx * 2, 64,
+               (uint32_t)Mp))
+      return cudaErrorInvalidValue;
+  } else {
     // image [copies][img_rows][kpad] f16 seen as {64, img_rows, copies, kpad/64}; a box covers
     // Mp rows (rows past img_rows read as zeros)
     const uint64_t d[4] = {64, (uint64_t)a.img_rows, (uint64_t)kXCopies, (uint64_t)(p.kpad / 64)};
@@ -155,6 +161,9 @@ cudaError_t launch_skinny2(int fmt, const Skinny2Plan& p, const Skinny2Args& a, 
   if (fmt == FMT_FP8)
     return p.mt == 1 ? launch2<FMT_FP8, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
                      : launch2<FMT_FP8, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);
+  if (fmt == FMT_BF16)
+    return p.mt == 1 ? launch2<FMT_BF16, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
+                     : launch2<FMT_BF16, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);
   return p.mt == 1 ? launch2<FMT_MXFP4, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
                    : launch2<FMT_MXFP4, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);
 }

@@ -25,7 +25,7 @@
 
 namespace ql {
 
-enum Fmt { FMT_INT8 = 0, FMT_FP8 = 1, FMT_MXFP4 = 2 };
+enum Fmt { FMT_INT8 = 0, FMT_FP8 = 1, FMT_MXFP4 = 2, FMT_BF16 = 3 };  // BF16: persistent kernel only
 enum Epi { EPI_INT8 = 0, EPI_LINEAR = 1, EPI_GATEUP = 2, EPI_DOWN = 3 };
 enum XKind { X_INT8 = 0, X_BF16 = 1 };
 

@@ -106,7 +106,7 @@ struct Skinny2Args {
 
 template <int FMT>
 struct S2Traits {
-  static constexpr int KPC = (FMT == FMT_MXFP4) ? 256 : 128;  // K elements per 128-byte chunk
+  static constexpr int KPC = (FMT == FMT_MXFP4) ? 256 : (FMT == FMT_BF16 ? 64 : 128);  // K per 128-byte chunk
   static constexpr int KPU = KPC * S2_CHUNKS;                  // K elements per unit
   static constexpr int NXB = KPU / 64;                         // 64-element activation slabs per unit
   static constexpr int SCB = (FMT == FMT_MXFP4) ? S2_ROWS * 8 * S2_CHUNKS : 0;  // scale bytes per unit
@@ -128,6 +128,11 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {

@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
   constexpr uint32_t STAGE = s2_stage_bytes<FMT, MT>();
   constexpr bool kInt = (FMT == FMT_INT8);
   constexpr bool kMoE = (KIND != S2_DENSE);
+  constexpr bool kBF16 = (FMT == FMT_BF16);  // activations loaded as they are: no image, no jobs
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
     *abort = 1;
   };
   // jobs that build the activation image, and how many of them the producers wait for
-  const int njob_rows = KIND == S2_MOE_DN ? a.offsets[a.E] : a.M;
+  const int njob_rows = KIND == S2_MOE_DN ? a.offsets[a.E] : (kBF16 ? 0 : a.M);
   const int nsl = s2_slices(max(njob_rows, 1), G);
   const unsigned need = (unsigned)(njob_rows * nsl);
 
@@ -134,9 +135,20 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
       }
     };
     if (n_units == 0) {
-      if (lane == 0) handoff();
+      if (lane == 0 && !kBF16) handoff();
       return;
     }
+    // activation tiles of unit kt: the image (4D) or, for BF16, the caller's x itself (2D boxes
+    // of 64 columns, rows past M and columns past K read as zeros)
+    auto load_x = [&](uint32_t dst, int ktx, int xrow_, uint64_t* bar) {
+      if constexpr (kBF16) {
+#pragma unroll
+        for (int j = 0; j < Tr::NXB; ++j)
+          tc::tma_load_2d(smem + (dst - tc::smem_u32(smem)) + j * X_BOX, &tmX, (ktx * Tr::NXB + j) * 64, 0, bar);
+      } else {
+        tma_load_4d(dst, &tmX, 0, xrow_, xcp, ktx * Tr::NXB, bar);
+      }
+    };
     bool ok = true;
     int issued = 0;
     // unit counters kept incrementally: no divisions in the loop
@@ -169,18 +181,20 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
           tc::tma_load_2d(smem + (size_t)slot * STAGE + W_CHUNK, &tmW2, kt * S2_WB + 128, rbl * S2_ROWS, &full[slot]);
         }
         if (i >= pre) {
-          tma_load_4d(st + W_BYTES, &tmX, 0, xrow, xcp, kt * Tr::NXB, &full[slot]);
+          load_x(st + W_BYTES, kt, xrow, &full[slot]);
         } else if (i == pre - 1) {
           // the activation image is written by this grid's consumer warps: wait for it, then
           // load the activation tiles of the stages already in flight.  On a timeout the
           // status is flagged and the loads still go out, so no stage waits forever.
-          handoff();
+          if constexpr (kBF16)
+            pdl_wait();  // x may come from the previous kernel
+          else
+            handoff();
           int ktj = (int)(s0 - (int64_t)rb_first * nk), rbj = rb_first;
           for (int j = 0; j < pre; ++j) {  // pre <= S: stage j is slot j
             const int uj = kMoE ? rbj / a.nb : 0;
             const uint32_t stj = tc::smem_u32(smem + (size_t)j * STAGE);
-            tma_load_4d(stj + W_BYTES, &tmX, 0, KIND == S2_MOE_DN ? uj * a.slot_rows : 0, xcp, ktj * Tr::NXB,
-                        &full[j]);
+            load_x(stj + W_BYTES, ktj, KIND == S2_MOE_DN ? uj * a.slot_rows : 0, &full[j]);
             if (++ktj == nk) {
               ktj = 0;
               ++rbj;
@@ -269,7 +283,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int col = 2 * t + e2 + 8 * m;
-        colf[m][e2] = col < cnt ? a.tokf[(KIND == S2_MOE_DN ? eu * a.slot_rows : 0) + col] : 0.f;
+        colf[m][e2] = col < cnt ? (kBF16 ? 1.f : a.tokf[(KIND == S2_MOE_DN ? eu * a.slot_rows : 0) + col]) : 0.f;
       }
     float rowf[2] = {1.f, 1.f}, rowb[2] = {0.f, 0.f};
     if constexpr (KIND == S2_DENSE) {
@@ -368,7 +382,19 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
 #pragma unroll
         for (int p = 0; p < 4; ++p)
           ldmatrix_x4(wt + sw128(lrow, (2 * p + lpc) * 16), q[p][0], q[p][1], q[p][2], q[p][3]);
-        if constexpr (FMT == FMT_MXFP4) {
+        if constexpr (FMT == FMT_BF16) {
+          // bf16 weights: q[p] is already the A fragment of the MMA over K 16p..16p+15 of the
+          // chunk (64 K = one activation slab); tokens' x at K 16p+2t.. and 16p+8+2t..
+#pragma unroll
+          for (int p = 0; p < 4; ++p)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              const uint32_t xs = xt + ck * X_BOX;
+              const uint32_t b0 = lds32(xs + sw128(g + 8 * m, 32 * p + 4 * t));
+              const uint32_t b1 = lds32(xs + sw128(g + 8 * m, 32 * p + 16 + 4 * t));
+              mma_bf16_16816(acc[m], q[p][0], q[p][1], q[p][2], q[p][3], b0, b1);
+            }
+        } else if constexpr (FMT == FMT_MXFP4) {
           // scale bytes of rows g and g+8 for the chunk's 8 groups
           const uint32_t sbase = st + W_BYTES + X_BYTES;
           const uint2 sa8 = lds64(sbase + (16 * w + g) * 16 + ck * 8);
