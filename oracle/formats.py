@@ -91,6 +91,33 @@ def e4m3_decode(codes) -> np.ndarray:
     return E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
 
 
+# ----------------------------------------------------------------------------------------
+# OCP FP8 E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits, IEEE-style: exponent 31 with
+# mantissa 0 is infinity, otherwise NaN; largest finite 57344.  [Z100] §二.2.2 names both
+# e4m3fn and e5m2 weights for the per-tensor / per-channel FP8 GEMV.
+# ----------------------------------------------------------------------------------------
+
+
+def e5m2_value(code: int) -> float:
+    s = (code >> 7) & 1
+    e = (code >> 2) & 0x1F
+    m = code & 0x3
+    if e == 0x1F:
+        mag = float("inf") if m == 0 else float("nan")
+    elif e == 0:
+        mag = (m / 4.0) * 2.0 ** -14
+    else:
+        mag = (1.0 + m / 4.0) * 2.0 ** (e - 15)
+    return -mag if s else mag
+
+
+E5M2_TABLE = np.array([e5m2_value(c) for c in range(256)], dtype=np.float64)
+
+
+def e5m2_decode(codes) -> np.ndarray:
+    return E5M2_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
 # non-negative finite magnitudes in code order 0x00..0x7E (monotone increasing)
 _E4M3_POS = E4M3_TABLE[:0x7F].copy()
 

@@ -35,6 +35,7 @@ from .formats import (
     e2m1_decode,
     e4m3_decode,
     e4m3_encode_rne_sat,
+    e5m2_decode,
     round_to_bf16,
     unpack_e2m1,
     ue8m0_decode,
@@ -152,6 +153,28 @@ def fp8_block(x, w_codes, w_scale_bytes, K, block_n=128, block_k=128, a_scale=No
         y += part * ws[None, :] * asc[:, None]
         a += apart * ws[None, :] * asc[:, None]
     return y, a
+
+
+# ----------------------------------------------------------------------------------------
+# FP8 weights with per-tensor / per-channel scales ([Z100] §二.2.2, the emulated FP8 GEMV:
+# e4m3fn or e5m2 codes, one fp32 scale per output channel or for the whole tensor, "the scale
+# is multiplied only once", after the dot product).
+#   y[m, n] = w_s[n] * sum_k x[m, k] * fp8(w[n, k])
+# ----------------------------------------------------------------------------------------
+
+
+def fp8_channel(x_bits, w_codes, w_fmt, w_s, K, rows=None):
+    """x_bits: bf16 [M, K]; w_codes: FP8 bytes [N, ldw] (first K used); w_fmt: "e4m3" or
+    "e5m2"; w_s: fp32 [N] (per channel) or [1] (per tensor).  Returns (y fp64 [M, R],
+    abs_sum fp64 [M, R]) with abs_sum = |w_s| sum_k |x w|, the float tolerance's scale."""
+    x = bf16_to_f64(np.asarray(x_bits)[:, :K])
+    w_codes = np.asarray(w_codes, dtype=np.uint8)
+    rows = np.arange(w_codes.shape[0]) if rows is None else np.asarray(rows)
+    dec = e4m3_decode if w_fmt == "e4m3" else e5m2_decode
+    w = dec(w_codes[rows, :K])
+    ws = np.asarray(w_s, dtype=np.float64)
+    s = ws[rows] if ws.size > 1 else np.full(rows.size, ws[0])
+    return (x @ w.T) * s[None, :], (np.abs(x) @ np.abs(w).T) * np.abs(s)[None, :]
 
 
 # ----------------------------------------------------------------------------------------

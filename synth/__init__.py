@@ -70,6 +70,23 @@ def fp8_block_case(M, N, K, seed=0, ldw=None, block_n=128, block_k=128, s_lo=118
 
 
 # ---------------------------------------------------------------- MXFP4 cases
+# the 248 finite E5M2 codes (exponent 31 is infinity or NaN)
+_E5M2_FINITE = np.array([c for c in range(256) if ((c >> 2) & 0x1F) != 0x1F], dtype=np.uint8)
+
+
+def fp8_channel_case(M, N, K, seed=0, ldw=None, w_fmt="e4m3", per_channel=True):
+    """FP8 weights with fp32 scales: codes uniform over the finite codes of the format [N, ldw]
+    (padding columns hold 0xFF, a NaN code in both formats), scales ~ U[2^-10, 2^-6] per channel
+    (or one per tensor), x ~ N(0,1) bf16 [M, K]."""
+    ldw = K if ldw is None else ldw
+    w = np.full((N, ldw), 0xFF, dtype=np.uint8)
+    table = _E4M3_FINITE if w_fmt == "e4m3" else _E5M2_FINITE
+    w[:, :K] = table[rng(seed, _W).integers(0, table.size, size=(N, K))]
+    ws = rng(seed, _WS).uniform(2.0 ** -10, 2.0 ** -6, size=N if per_channel else 1).astype(np.float32)
+    x = bf16_normal(rng(seed, _X), (M, K))
+    return {"x": x, "w": w, "w_s": ws}
+
+
 def bf16_dense_case(M, N, K, seed=0, ldw=None):
     """BF16 dense weights: w ~ N(0, 0.05^2) bf16 [N, ldw] (padding columns hold a NaN, so a
     kernel that reads past K shows it), x ~ N(0,1) bf16 [M, K]."""

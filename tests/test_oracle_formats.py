@@ -45,6 +45,50 @@ def test_e4m3_exhaustive_vs_ml_dtypes():
     assert np.array_equal(lib[ok], ours[ok])
 
 
+def _ref_e5m2(code):
+    # closed form written independently: E5M2 is the top byte of an IEEE binary16
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 2) & 0x1F, code & 3
+    if e == 31:
+        return sign * math.inf if m == 0 else math.nan
+    return sign * (math.ldexp(m, -16) if e == 0 else math.ldexp(4 + m, e - 17))
+
+
+def test_e5m2_exhaustive_closed_form():
+    for c in range(256):
+        want, got = _ref_e5m2(c), F.e5m2_decode(np.uint8(c))
+        if math.isnan(want):
+            assert np.isnan(got), c
+        else:
+            assert got == want, (c, got, want)
+    fin = F.E5M2_TABLE[np.isfinite(F.E5M2_TABLE)]
+    assert fin.size == 248 and fin.max() == 57344.0
+    assert F.e5m2_decode(np.uint8(0x01)) == 2.0 ** -16     # smallest subnormal
+    assert F.e5m2_decode(np.uint8(0x3C)) == 1.0
+
+
+def test_e5m2_is_the_high_byte_of_float16():
+    # an independent library route: code c is the binary16 with bits c << 8
+    codes = np.arange(256, dtype=np.uint16)
+    lib = (codes << 8).astype(np.uint16).view(np.float16).astype(np.float64)
+    ours = F.e5m2_decode(codes.astype(np.uint8))
+    assert np.array_equal(np.isnan(lib), np.isnan(ours))
+    ok = ~np.isnan(lib)
+    assert np.array_equal(lib[ok], ours[ok])
+
+
+def test_e5m2_vs_torch():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e5m2"):
+        pytest.skip("torch without float8_e5m2")
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = codes.view(torch.float8_e5m2).to(torch.float64).numpy()
+    ours = F.e5m2_decode(np.arange(256, dtype=np.uint8))
+    assert np.array_equal(np.isnan(lib), np.isnan(ours))
+    ok = ~np.isnan(lib)
+    assert np.array_equal(lib[ok], ours[ok])
+
+
 def test_e2m1_exhaustive():
     want = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
     assert list(F.E2M1_TABLE[:8]) == want

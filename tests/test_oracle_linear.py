@@ -224,3 +224,50 @@ def test_bf16_linear_row_subset_and_transpose():
     yy, _ = Q.bf16_linear(sq["x"], sq["w"], 3)
     wrong = F.bf16_to_f64(sq["x"]) @ F.bf16_to_f64(sq["w"])
     assert not np.allclose(yy, wrong)
+
+
+# ------------------------------------------------------------------ FP8 per-tensor / per-channel
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_channel_rational_brute_force(fmt):
+    # exact rational dot products; the oracle's fp64 evaluation may round only within the
+    # fp64 summation bound (E5M2's 31-binade range can exceed 53 bits in a 16-term sum)
+    c = synth.fp8_channel_case(2, 4, 16, seed=11, w_fmt=fmt)
+    y, a = Q.fp8_channel(c["x"], c["w"], fmt, c["w_s"], 16)
+    dec = F.e4m3_decode if fmt == "e4m3" else F.e5m2_decode
+    xv, wv = F.bf16_to_f64(c["x"]), dec(c["w"][:, :16])
+    for m in range(2):
+        for n in range(4):
+            s = Fraction(float(c["w_s"][n]))
+            terms = [Fraction(float(xv[m, k])) * Fraction(float(wv[n, k])) for k in range(16)]
+            ref = s * sum(terms)
+            bound = 18 * Fraction(2) ** -53 * abs(s) * sum(abs(t) for t in terms)
+            assert abs(Fraction(float(y[m, n])) - ref) <= bound
+            assert abs(Fraction(float(a[m, n])) - abs(s) * sum(abs(t) for t in terms)) <= bound
+
+
+def test_fp8_channel_per_tensor_is_uniform_per_channel():
+    c = synth.fp8_channel_case(3, 6, 40, seed=12, per_channel=False)
+    y1, a1 = Q.fp8_channel(c["x"], c["w"], "e4m3", c["w_s"], 40)
+    y2, a2 = Q.fp8_channel(c["x"], c["w"], "e4m3", np.full(6, c["w_s"][0], np.float32), 40)
+    assert np.array_equal(y1, y2) and np.array_equal(a1, a2)
+
+
+def test_fp8_channel_unit_scale_is_block_path_with_unit_blocks():
+    # with every scale 1 the per-channel formula equals the 128x128 block formula at scale 2^0
+    c = synth.fp8_channel_case(2, 130, 300, seed=13)
+    y, _ = Q.fp8_channel(c["x"], c["w"], "e4m3", np.ones(130, np.float32), 300)
+    sb = np.full((2, 3), 127, np.uint8)
+    yb, _ = Q.fp8_block(F.bf16_to_f64(c["x"]), c["w"], sb, 300)
+    assert np.allclose(y, yb, rtol=1e-13, atol=0)
+
+
+def test_fp8_channel_scale_index_and_padding():
+    # a scale on one channel changes only that output column; padding past K is never read
+    c = synth.fp8_channel_case(2, 5, 24, seed=14, ldw=40, w_fmt="e5m2")
+    ws = np.ones(5, np.float32)
+    y0, _ = Q.fp8_channel(c["x"], c["w"], "e5m2", ws, 24)
+    ws[3] = 4.0
+    y1, _ = Q.fp8_channel(c["x"], c["w"], "e5m2", ws, 24)
+    assert np.array_equal(y1[:, [0, 1, 2, 4]], y0[:, [0, 1, 2, 4]])
+    assert np.array_equal(y1[:, 3], 4.0 * y0[:, 3])
+    assert np.all(np.isfinite(y0))
