@@ -11,7 +11,8 @@ weights from HBM (no call finds them in the 129 MB L2).  Activations are small a
 wherever the previous write left them, as in a decode step.
 
 --config selects the other workloads (c0: INT8 M=1 N=512 K=1024; c2: FP8 128x128 block;
-c3: MXFP4 MoE E=256 H=4096 I=2048 top-8; c4: tcgen05 FP8/MXFP4 M=64..256).
+c3: MXFP4 MoE E=256 H=4096 I=2048 top-8; c4: tcgen05 FP8/MXFP4 M=64..256;
+n2: FP8 E4M3 per-channel scales; n4: BF16 unquantised weights).
 --impl reference times the CPU oracle on a bounded row sample of the same workload.
 Under torchrun each rank runs an independent replica (the layer needs no exchange).
 """
@@ -43,6 +44,24 @@ C4_MS = [64, 128, 256]
 ROTATE = 6  # weight copies per shape (>= 3 x 44.6 MB between reuses)
 
 
+# one name per workload, used by both arms
+WORKLOADS = {
+    "c0": "INT8 W8A8 GEMV M=1 N=512 K=1024",
+    "c1": "INT8 W8A8 skinny GEMM, 27B-class decode shapes (N,K) in {(17408,5120),(5120,17408),(10240,5120)} "
+          "x M in {1,2,4,8,16}",
+    "c2": "FP8 E4M3 128x128 UE8M0 block-scaled GEMV, bf16 activations, (N,K) in {(17408,5120),(5120,17408)} "
+          "x M in {1,4,8,16}",
+    "c3": "MXFP4 MoE decode: 256 experts, hidden 4096, intermediate 2048, top-8, M in 1..9",
+    "c4": "tcgen05 block-scaled GEMM, 1x128 E4M3 activations, FP8 128x128 and MXFP4 weights, "
+          "(N,K)=(17408,5120), M in {64,128,256}",
+    "n2": "FP8 E4M3 per-channel-scaled decode GEMV, bf16 activations, (N,K) in "
+          "{(17408,5120),(5120,17408),(10240,5120)} x M in {1,4,16}",
+    "n4": "BF16 dense decode GEMV (unquantised weights), (N,K) in {(17408,5120),(5120,17408)} x M in {1,4,16}",
+}
+# the arithmetic type of each workload's weights
+DTYPES = {"c0": "int8", "c1": "int8", "c2": "fp8", "c3": "fp4", "c4": "fp8/fp4", "n2": "fp8", "n4": "bf16"}
+
+
 # ----------------------------------------------------------------------------- bytes / flops
 def bytes_int8(M, N, K):
     return N * K + 4 * N + 2 * M * K + 2 * M * N
@@ -50,6 +69,10 @@ def bytes_int8(M, N, K):
 
 def bytes_fp8(M, N, K):
     return N * K + (-(-N // 128)) * (-(-K // 128)) + 2 * M * K + 2 * M * N
+
+
+def bytes_fp8c(M, N, K, per_channel=True):
+    return N * K + (4 * N if per_channel else 4) + 2 * M * K + 2 * M * N
 
 
 def bytes_bf16(M, N, K):
@@ -188,15 +211,13 @@ def build_c1(ql, torch, shapes=C1_SHAPES, Ms=C1_MS, name="c1"):
 
             calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": bytes_int8(M, N, K), "flops": 2 * M * N * K,
                           "x": x, "y": y, "kind": "int8"})
-    cfg = {"workload": "INT8 W8A8 skinny GEMM, 27B-class decode shapes (N,K) in "
-                       "{(17408,5120),(5120,17408),(10240,5120)} x M in {1,2,4,8,16}",
-           "shapes": [list(s) for s in shapes], "M": Ms}
+    cfg = {"workload": WORKLOADS[name], "shapes": [list(s) for s in shapes], "M": Ms}
     return Workload(name, calls, len(calls), cfg)  # one fused launch per call
 
 
 def build_c0(ql, torch):
     w = build_c1(ql, torch, shapes=[(512, 1024)], Ms=[1], name="c0")
-    w.cfg = {"workload": "INT8 W8A8 GEMV M=1 N=512 K=1024", "shapes": [[512, 1024]], "M": [1]}
+    w.cfg = {"workload": WORKLOADS["c0"], "shapes": [[512, 1024]], "M": [1]}
     return w
 
 
@@ -221,8 +242,7 @@ def build_c2(ql, torch):
 
             calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": bytes_fp8(M, N, K), "flops": 2 * M * N * K,
                           "x": x, "y": y, "kind": "fp8"})
-    cfg = {"workload": "FP8 E4M3 128x128 UE8M0 block-scaled GEMV, bf16 activations, (N,K) in "
-                       "{(17408,5120),(5120,17408)} x M in {1,4,8,16}"}
+    cfg = {"workload": WORKLOADS["c2"]}
     return Workload("c2", calls, len(calls), cfg)
 
 
@@ -250,7 +270,7 @@ def build_c3(ql, torch):
         b = uniq * bytes_moe_expert(H, I) + 2 * M * H * 2 + 2 * M * E
         calls.append({"fn": call, "M": M, "N": H, "K": I, "bytes": b, "flops": 2 * M * topk * 3 * H * I,
                       "x": sets[0][0], "y": y, "kind": "moe", "unique_experts": uniq})
-    cfg = {"workload": "MXFP4 MoE decode: 256 experts, hidden 4096, intermediate 2048, top-8, M in 1..9",
+    cfg = {"workload": WORKLOADS["c3"],
            "bytes": "unique touched experts x 13369344 B + x + logits + y"}
     return Workload("c3", calls, 4 * len(calls), cfg)
 
@@ -289,8 +309,7 @@ def build_c4(ql, torch):
                 b = bytes_mxfp4(M, N, K)
             calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": b, "flops": 2 * M * N * K, "x": x, "y": y,
                           "kind": kind + "_tcgen05"})
-    cfg = {"workload": "tcgen05 block-scaled GEMM, 1x128 E4M3 activations, FP8 128x128 and MXFP4 weights, "
-                       "(N,K)=(17408,5120), M in {64,128,256}"}
+    cfg = {"workload": WORKLOADS["c4"]}
     return Workload("c4", calls, 2 * len(calls), cfg)
 
 
@@ -318,17 +337,49 @@ def build_n4(ql, torch):
 
             calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": bytes_bf16(M, N, K), "flops": 2 * M * N * K,
                           "x": x, "y": y, "kind": "bf16"})
-    cfg = {"workload": "BF16 dense decode GEMV (unquantised weights), (N,K) in {(17408,5120),(5120,17408)} "
-                       "x M in {1,4,16}"}
+    cfg = {"workload": WORKLOADS["n4"]}
     return Workload("n4", calls, len(calls), cfg)
 
 
-BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4": build_c4, "n4": build_n4}
+N2_SHAPES = C1_SHAPES
+N2_MS = [1, 4, 16]
+
+
+def build_n2(ql, torch):
+    """FP8 weights with one fp32 scale per output channel (a NEXT row: e4m3fn codes, the scale
+    applied once at the end), on the 27B-class decode shapes the pages time the emulated FP8
+    GEMV on."""
+    calls = []
+    weights = {}
+    for (N, K) in N2_SHAPES:
+        c = synth.fp8_channel_case(1, N, K, seed=0)
+        w0 = torch.from_numpy(c["w"]).cuda()
+        weights[(N, K)] = ([w0] + [w0.clone() for _ in range(ROTATE - 1)], torch.from_numpy(c["w_s"]).cuda(),
+                           {"i": 0})
+    for M in N2_MS:
+        for (N, K) in N2_SHAPES:
+            ws, sc, state = weights[(N, K)]
+            x = dev_bf16(synth.fp8_channel_case(M, 1, K, seed=1)["x"], torch)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+
+            def call(ws=ws, sc=sc, x=x, y=y, state=state):
+                w = ws[state["i"] % ROTATE]
+                state["i"] += 1
+                ql.qlinear_fp8(x, w, sc, "e4m3", out=y)
+
+            calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": bytes_fp8c(M, N, K), "flops": 2 * M * N * K,
+                          "x": x, "y": y, "kind": "fp8_channel"})
+    cfg = {"workload": WORKLOADS["n2"]}
+    return Workload("n2", calls, len(calls), cfg)
+
+
+BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4": build_c4, "n2": build_n2,
+            "n4": build_n4}
 
 _SKINNY = ("skinny2_kernel (one launch per call: activation preparation + weight-streaming GEMM); "
            "achieved = algorithmic bytes per call / CUDA-event time per call (graphs of 32 back-to-back "
            "calls), aggregated over the step's calls")
-KERNEL_DESC = {"c0": _SKINNY, "c1": _SKINNY, "c2": _SKINNY, "n4": _SKINNY,
+KERNEL_DESC = {"c0": _SKINNY, "c1": _SKINNY, "c2": _SKINNY, "n2": _SKINNY, "n4": _SKINNY,
                "c3": "MoE launches per call (routing, gate_up, down, combine); bytes of the touched experts / "
                      "event time per call",
                "c4": "tcgen05 block-scaled GEMM + its activation-quantisation launch; bytes / event time per call"}
@@ -464,6 +515,16 @@ def oracle_sample(config, rows_per_call):
             sec += time.perf_counter() - t
             done += len(np.unique(ids)) * 2 * len(cols) * (H // 2 + H // 32)
         desc = f"MoE oracle routing + gate_up on {rows_per_call} intermediate rows for M=1 and M=9"
+    elif config == "n2":
+        for (N, K) in N2_SHAPES:
+            c = _case(("fp8c", N, K), lambda: synth.fp8_channel_case(16, N, K, seed=0))
+            rows = np.arange(min(rows_per_call, N))
+            for M in N2_MS:
+                t = time.perf_counter()
+                Q.fp8_channel(c["x"][:M], c["w"], "e4m3", c["w_s"], K, rows=rows)
+                sec += time.perf_counter() - t
+                done += bytes_fp8c(M, len(rows), K)
+        desc = f"FP8 per-channel oracle on the first {rows_per_call} output rows of each of the 9 calls"
     elif config == "n4":
         for (N, K) in C2_SHAPES:
             c = _case(("bf16", N, K), lambda: synth.bf16_dense_case(16, N, K, seed=0))
@@ -543,22 +604,12 @@ def run_reference(args, ws, rank):
     val = b / t / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
-            "data": "synthetic", "config": {"workload": BUILD_CFG_NAMES[args.config]},
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPES[args.config],
+            "data": "synthetic", "config": {"workload": WORKLOADS[args.config]},
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": desc + f" ({rows} rows per call per step)"},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
-
-
-BUILD_CFG_NAMES = {
-    "c0": "INT8 W8A8 GEMV M=1 N=512 K=1024",
-    "c1": "INT8 W8A8 skinny GEMM, 27B-class decode shapes (N,K) in {(17408,5120),(5120,17408),(10240,5120)} "
-          "x M in {1,2,4,8,16}",
-    "c2": "FP8 E4M3 128x128 block-scaled GEMV (17408,5120),(5120,17408) x M in {1,4,8,16}",
-    "c3": "MXFP4 MoE decode E=256 H=4096 I=2048 top-8, M in 1..9",
-    "c4": "tcgen05 block-scaled GEMM FP8/MXFP4, (17408,5120), M in {64,128,256}",
-}
 
 
 def main():
@@ -579,7 +630,8 @@ def main():
 
     import torch
     if args.steps is None:
-        args.steps = {"c0": 20000, "c1": 4000, "c2": 4000, "c3": 2000, "c4": 2000, "n4": 2000}[args.config]
+        args.steps = {"c0": 20000, "c1": 4000, "c2": 4000, "c3": 2000, "c4": 2000, "n2": 3000,
+                      "n4": 2000}[args.config]
     torch.cuda.set_device(local)
     pg = None
     if ws > 1:
@@ -641,9 +693,7 @@ def main():
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": {"c0": "int8", "c1": "int8", "c2": "fp8", "c3": "fp4", "c4": "fp8/fp4",
-                                           "n4": "bf16"}[
-                args.config], "data": "synthetic",
+            "vs_baseline": None, "dtype": DTYPES[args.config], "data": "synthetic",
             "config": dict(wl.cfg, parallelism=f"replicas x{ws}", l2="weights rotate over 6 copies per shape "
                                                                    "(inputs larger than L2)"),
             "us_per_call_mean": round(ms_step * 1e3 / len(wl.calls), 3),

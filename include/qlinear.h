@@ -56,7 +56,12 @@ typedef enum {
 } ql_status;
 
 /* operation ids for ql_workspace_bytes */
-enum { QL_OP_INT8_W8A8 = 1, QL_OP_FP8_BLOCK = 2, QL_OP_MXFP4 = 3, QL_OP_MOE_MXFP4 = 4, QL_OP_BF16 = 5 };
+enum { QL_OP_INT8_W8A8 = 1, QL_OP_FP8_BLOCK = 2, QL_OP_MXFP4 = 3, QL_OP_MOE_MXFP4 = 4, QL_OP_BF16 = 5,
+       QL_OP_FP8_CHANNEL = 6 };
+
+/* FP8 weight code formats of qlinear_fp8 */
+enum { QL_FP8_E4M3 = 0 /* e4m3fn: bias 7, no infinities, S.1111.111 is NaN */,
+       QL_FP8_E5M2 = 1 /* e5m2: bias 15, IEEE-style infinities and NaNs      */ };
 
 /* activation modes of the FP8-block and MXFP4 linears */
 enum {
@@ -76,7 +81,8 @@ enum {
   QL_PATH_MXFP4_SKINNY = 4,    /* MXFP4 skinny GEMM, bf16 activations                       */
   QL_PATH_MXFP4_TCGEN05 = 5,   /* 1x128 act quant + tcgen05 block-scaled GEMM (E4M3 x E2M1) */
   QL_PATH_MOE_MXFP4 = 6,       /* routing + dispatch + gate_up/SiLU + down + combine         */
-  QL_PATH_BF16_SKINNY = 7      /* BF16 skinny GEMM (unquantised weights)                    */
+  QL_PATH_BF16_SKINNY = 7,     /* BF16 skinny GEMM (unquantised weights)                    */
+  QL_PATH_FP8_CHANNEL_SKINNY = 8 /* FP8 skinny GEMM, per-channel / per-tensor fp32 scale     */
 };
 
 /* device status flags (bitmask) */
@@ -173,6 +179,29 @@ QL_API ql_status qlinear_mxfp4(const uint16_t* x, int64_t M, int64_t K, int64_t 
                         uint8_t* aq_out, uint8_t* as_out,
                         void* workspace, size_t workspace_bytes, ql_stream_t stream,
                         int* path_out);
+
+/*
+ * FP8 weights with one fp32 scale per output channel or per tensor ([Z100] §二.2.2, the
+ * emulated FP8 GEMV: e4m3fn or e5m2 codes widened exactly, the scale applied once to the
+ * finished dot product):
+ *   y[m,n] = bf16( w_scale[n or 0] * sum_k x[m,k] * fp8(w[n,k]) ) (+ bias, added after the
+ *   cast and rounded again)
+ * x: bf16 [M, ldx] (device); w: FP8 codes [N, ldw] (device, K used, padded rows allowed);
+ * w_fmt: QL_FP8_E4M3 or QL_FP8_E5M2; w_scale: fp32 [w_scale_len] (device), w_scale_len = N
+ * (per channel) or 1 (per tensor); bias: bf16 [N] or null; y: bf16 [M, ldy] (device).  The
+ * caller owns every buffer; nothing is retained after the call returns.  Codes must be finite
+ * (NaN / infinity codes propagate through the sum).  Runs the persistent skinny kernel 16
+ * tokens at a time, bf16 activations.
+ * Requires K % 16 == 0, ldx % 8 == 0, ldw % 16 == 0, 16-byte aligned x and w, ldy >= N;
+ * returns QL_ERR_INVALID_ARG / QL_ERR_ALIGNMENT / QL_ERR_UNSUPPORTED before any launch
+ * otherwise.  workspace: ql_workspace_bytes(QL_OP_FP8_CHANNEL, M, N, K, 0, 0) bytes, zeroed once.
+ */
+QL_API ql_status qlinear_fp8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                      const uint8_t* w, int64_t N, int64_t ldw, int w_fmt,
+                      const float* w_scale, int64_t w_scale_len,
+                      const uint16_t* bias, uint16_t* y, int64_t ldy,
+                      void* workspace, size_t workspace_bytes, ql_stream_t stream,
+                      int* path_out);
 
 /*
  * BF16 dense decode GEMV, unquantised weights ([Z100] §二.2.3, the bf16 route: bf16 widened to

@@ -157,8 +157,8 @@ def fp8_block(x, w_codes, w_scale_bytes, K, block_n=128, block_k=128, a_scale=No
 
 # ----------------------------------------------------------------------------------------
 # FP8 weights with per-tensor / per-channel scales ([Z100] §二.2.2, the emulated FP8 GEMV:
-# e4m3fn or e5m2 codes, one fp32 scale per output channel or for the whole tensor, "the scale
-# is multiplied only once", after the dot product).
+# e4m3fn or e5m2 codes, one fp32 scale per output channel or for the whole tensor, applied a
+# single time to the finished dot product).
 #   y[m, n] = w_s[n] * sum_k x[m, k] * fp8(w[n, k])
 # ----------------------------------------------------------------------------------------
 

@@ -20,7 +20,8 @@ from ._build import LIB as _LIB_PATH
 __all__ = [
     "lib", "QLError", "qlinear_int8_w8a8", "qlinear_fp8_block", "qlinear_mxfp4", "moe_mxfp4_grouped",
     "workspace_bytes", "Workspace", "read_device_status", "set_wait_limit",
-    "OP_INT8_W8A8", "OP_FP8_BLOCK", "OP_MXFP4", "OP_MOE_MXFP4", "OP_BF16", "qlinear_bf16", "ACT_BF16", "ACT_E4M3_1X128", "PATHS",
+    "OP_INT8_W8A8", "OP_FP8_BLOCK", "OP_MXFP4", "OP_MOE_MXFP4", "OP_BF16", "OP_FP8_CHANNEL", "qlinear_bf16",
+    "qlinear_fp8", "FP8_E4M3", "FP8_E5M2", "ACT_BF16", "ACT_E4M3_1X128", "PATHS",
 ]
 
 if not os.path.exists(_LIB_PATH):
@@ -51,6 +52,9 @@ lib.qlinear_fp8_block.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _
 lib.qlinear_bf16.restype = _int
 lib.qlinear_bf16.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _i64, _vp, _sz, _vp,
                              ctypes.POINTER(_int)]
+lib.qlinear_fp8.restype = _int
+lib.qlinear_fp8.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _int, _vp, _i64, _vp, _vp, _i64, _vp, _sz,
+                            _vp, _ip]
 lib.qlinear_mxfp4.restype = _int
 lib.qlinear_mxfp4.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _int, _vp, _vp, _i64,
                               _vp, _vp, _vp, _sz, _vp, _ip]
@@ -58,10 +62,11 @@ lib.moe_mxfp4_grouped.restype = _int
 lib.moe_mxfp4_grouped.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _int, _int, _int, _vp, _vp, _vp, _vp, _i64,
                                   _vp, _vp, _vp, _vp, _vp, _sz, _vp, _ip]
 
-OP_INT8_W8A8, OP_FP8_BLOCK, OP_MXFP4, OP_MOE_MXFP4, OP_BF16 = 1, 2, 3, 4, 5
+OP_INT8_W8A8, OP_FP8_BLOCK, OP_MXFP4, OP_MOE_MXFP4, OP_BF16, OP_FP8_CHANNEL = 1, 2, 3, 4, 5, 6
+FP8_E4M3, FP8_E5M2 = 0, 1
 ACT_BF16, ACT_E4M3_1X128 = 0, 1
 PATHS = {0: "none", 1: "int8_skinny", 2: "fp8_skinny", 3: "fp8_tcgen05", 4: "mxfp4_skinny",
-         5: "mxfp4_tcgen05", 6: "moe_mxfp4", 7: "bf16_skinny"}
+         5: "mxfp4_tcgen05", 6: "moe_mxfp4", 7: "bf16_skinny", 8: "fp8_channel_skinny"}
 
 
 class QLError(RuntimeError):
@@ -213,6 +218,29 @@ def qlinear_bf16(x, w, bias=None, *, debug=False, out=None, workspace=None, stre
     path = ctypes.c_int(0)
     _check(lib.qlinear_bf16(_ptr(x), M, K, x.stride(0), _ptr(w), N, w.stride(0), _ptr(bias), _ptr(y), y.stride(0),
                             _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(path)), "qlinear_bf16")
+    if debug:
+        return y, PATHS[path.value]
+    return y
+
+
+def qlinear_fp8(x, w, w_scale, w_fmt="e4m3", bias=None, *, debug=False, out=None, workspace=None, stream=None):
+    """y = bf16(w_scale[n or 0] * sum_k x w) (+ bias) on FP8 weight codes.  x: bf16 [M, K];
+    w: uint8 FP8 codes [N, >=K] (row stride w.stride(0)); w_fmt: "e4m3" or "e5m2"; w_scale:
+    fp32 [N] (per channel) or [1] (per tensor).  With debug=True returns (y, path)."""
+    _bf16(x, "x")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.dtype != torch.uint8 or w.stride(1) != 1 or x.stride(1) != 1:
+        raise TypeError("w must be uint8 FP8 codes with unit inner stride; x must have unit inner stride")
+    if w_scale.dtype != torch.float32:
+        raise TypeError("w_scale must be float32")
+    fmt = {"e4m3": FP8_E4M3, "e5m2": FP8_E5M2}[w_fmt]
+    y = out if out is not None else torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    ws = _ws(x.device, workspace_bytes(OP_FP8_CHANNEL, M, N, K), stream, workspace)
+    path = ctypes.c_int(0)
+    _check(lib.qlinear_fp8(_ptr(x), M, K, x.stride(0), _ptr(w), N, w.stride(0), fmt, _ptr(w_scale), w_scale.numel(),
+                           _ptr(bias), _ptr(y), y.stride(0), _ptr(ws), ws.numel(), _stream(stream),
+                           ctypes.byref(path)), "qlinear_fp8")
     if debug:
         return y, PATHS[path.value]
     return y

@@ -290,6 +290,8 @@ size_t ql_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int to
     }
     case QL_OP_BF16:
       return dense2_layout(FMT_BF16, Mc, N, K, 128).total;
+    case QL_OP_FP8_CHANNEL:
+      return dense2_layout(FMT_F8E4C, Mc, N, K, 128).total;  // E4M3 and E5M2 lay out alike
     case QL_OP_MOE_MXFP4: {
       if (E <= 0 || topk <= 0) return 0;
       const size_t a = moe_layout(M, N, K, E, topk).total, b = moe2_layout(M, N, K, E, topk).total;
@@ -459,6 +461,39 @@ ql_status qlinear_fp8_block(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
   if (e != cudaSuccess) return cuda_status(e);
   if (path_out) *path_out = QL_PATH_FP8_TCGEN05;
   return QL_OK;
+}
+
+// ------------------------------------------------------------------ FP8 per channel / per tensor
+ql_status qlinear_fp8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const uint8_t* w, int64_t N, int64_t ldw,
+                      int w_fmt, const float* w_scale, int64_t w_scale_len, const uint16_t* bias, uint16_t* y,
+                      int64_t ldy, void* workspace, size_t workspace_bytes, ql_stream_t stream, int* path_out) {
+  if (path_out) *path_out = QL_PATH_NONE;
+  if (!x || !w || !w_scale || !y) return QL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldx < K || ldw < K || ldy < N) return QL_ERR_INVALID_ARG;
+  if (w_fmt != QL_FP8_E4M3 && w_fmt != QL_FP8_E5M2) return QL_ERR_INVALID_ARG;
+  if (w_scale_len != 1 && w_scale_len != N) return QL_ERR_INVALID_ARG;
+  if (M > 65535 || N > (1 << 30) || K > (1 << 28)) return QL_ERR_UNSUPPORTED;
+  if (K % 16 != 0 || cdiv(N, S2_ROWS) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
+  if (!al16(x) || !al16(w) || ldx % 8 != 0 || ldw % 16 != 0) return QL_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < ql_workspace_bytes(QL_OP_FP8_CHANNEL, M, N, K, 0, 0)) return QL_ERR_WORKSPACE;
+  if (!al16(workspace)) return QL_ERR_ALIGNMENT;
+  Dense2Call d = {};
+  d.fmt = w_fmt == QL_FP8_E4M3 ? FMT_F8E4C : FMT_F8E5C;
+  d.x = x;
+  d.M = M;
+  d.K = K;
+  d.ldx = ldx;
+  d.w = w;
+  d.N = N;
+  d.ldw = ldw;
+  d.w_scale = w_scale;
+  d.w_scale_len = w_scale_len;
+  d.bias = bias;
+  d.y = y;
+  d.ldy = ldy;
+  const ql_status s = run_dense2(d, workspace, (cudaStream_t)stream);
+  if (s == QL_OK && path_out) *path_out = QL_PATH_FP8_CHANNEL_SKINNY;
+  return s;
 }
 
 // ------------------------------------------------------------------ BF16 dense

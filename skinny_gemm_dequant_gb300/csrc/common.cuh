@@ -60,6 +60,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
   return r;
 }
 
+// two E5M2 bytes (low byte -> low lane) to an exact f16x2 (E5M2 is a subset of f16)
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint16_t two) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(two));
+  return r;
+}
+
 // one byte holding two E2M1 codes (low nibble -> low lane) to an exact f16x2
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
   uint32_t r;

@@ -164,6 +164,12 @@ cudaError_t launch_skinny2(int fmt, const Skinny2Plan& p, const Skinny2Args& a, 
   if (fmt == FMT_BF16)
     return p.mt == 1 ? launch2<FMT_BF16, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
                      : launch2<FMT_BF16, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);
+  if (fmt == FMT_F8E4C)
+    return p.mt == 1 ? launch2<FMT_F8E4C, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
+                     : launch2<FMT_F8E4C, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);
+  if (fmt == FMT_F8E5C)
+    return p.mt == 1 ? launch2<FMT_F8E5C, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
+                     : launch2<FMT_F8E5C, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);
   return p.mt == 1 ? launch2<FMT_MXFP4, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
                    : launch2<FMT_MXFP4, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);
 }

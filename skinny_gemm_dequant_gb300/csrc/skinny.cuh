@@ -25,7 +25,9 @@
 
 namespace ql {
 
-enum Fmt { FMT_INT8 = 0, FMT_FP8 = 1, FMT_MXFP4 = 2, FMT_BF16 = 3 };  // BF16: persistent kernel only
+// BF16 and the per-channel FP8 formats (E4M3 / E5M2 codes, fp32 scale per channel or tensor)
+// run on the persistent kernel only
+enum Fmt { FMT_INT8 = 0, FMT_FP8 = 1, FMT_MXFP4 = 2, FMT_BF16 = 3, FMT_F8E4C = 4, FMT_F8E5C = 5 };
 enum Epi { EPI_INT8 = 0, EPI_LINEAR = 1, EPI_GATEUP = 2, EPI_DOWN = 3 };
 enum XKind { X_INT8 = 0, X_BF16 = 1 };
 

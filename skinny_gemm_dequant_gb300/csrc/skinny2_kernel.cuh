@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
   constexpr bool kInt = (FMT == FMT_INT8);
   constexpr bool kMoE = (KIND != S2_DENSE);
   constexpr bool kBF16 = (FMT == FMT_BF16);  // activations loaded as they are: no image, no jobs
+  constexpr bool kF8C = (FMT == FMT_F8E4C || FMT == FMT_F8E5C);  // FP8 codes, one scale per channel
+  constexpr bool kRowScale = kInt || kF8C;                         // fp32 w_scale applied once at the end
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int row = min(row_w + g + 8 * e2, a.N - 1);
-        if (kInt) rowf[e2] = a.w_scale[a.w_scale_len > 1 ? row : 0];
+        if (kRowScale) rowf[e2] = a.w_scale[a.w_scale_len > 1 ? row : 0];
         if (a.bias) rowb[e2] = bf16_bits_to_f32(a.bias[row]);
       }
     }
@@ -315,6 +317,8 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
             const int32_t v = __float_as_int(res[m][r]);
             if (a.acc_out) a.acc_out[(int64_t)col * a.N + row] = v;
             yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)v, colf[m][r & 1]), rowf[r >> 1]));
+          } else if constexpr (kF8C) {
+            yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn(res[m][r], colf[m][r & 1]), rowf[r >> 1]));
           } else {
             yb = f32_to_bf16_rn(res[m][r] * colf[m][r & 1]);
           }
@@ -366,8 +370,9 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
       }
       const uint32_t st = tc::smem_u32(smem + (size_t)slot * STAGE);
       const uint32_t xt = st + W_BYTES;
-      // INT8: the unit's sums in two fp32 chains; every partial sum is an integer of at most
-      // 256 x 127 x 127 < 2^24 in magnitude, so they are exact and convert once per unit
+      // INT8 and per-channel FP8: the unit's sums in two fp32 chains.  For INT8 every partial sum
+      // is an integer of at most 256 x 127 x 127 < 2^24 in magnitude, so they are exact and
+      // convert once per unit
       float ui[2][MT][4];
 #pragma unroll
       for (int e = 0; e < 2; ++e)
@@ -436,6 +441,31 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
               acc[m][3] = fmaf(blk[m][3], fb, acc[m][3]);
             }
           }
+        } else if constexpr (kF8C) {
+          // FP8 codes to exact f16 and straight into the unit's two fp32 chains: the channel
+          // scale is applied once, in the epilogue
+#pragma unroll
+          for (int pc = 0; pc < 8; ++pc) {
+            const uint32_t qa = q[pc >> 1][2 * (pc & 1)], qb = q[pc >> 1][2 * (pc & 1) + 1];
+            uint32_t a0, a1, a2, a3;
+            if constexpr (FMT == FMT_F8E4C) {
+              a0 = e4m3x2_to_f16x2((uint16_t)(qa & 0xFFFFu));
+              a2 = e4m3x2_to_f16x2((uint16_t)(qa >> 16));
+              a1 = e4m3x2_to_f16x2((uint16_t)(qb & 0xFFFFu));
+              a3 = e4m3x2_to_f16x2((uint16_t)(qb >> 16));
+            } else {
+              a0 = e5m2x2_to_f16x2((uint16_t)(qa & 0xFFFFu));
+              a2 = e5m2x2_to_f16x2((uint16_t)(qa >> 16));
+              a1 = e5m2x2_to_f16x2((uint16_t)(qb & 0xFFFFu));
+              a3 = e5m2x2_to_f16x2((uint16_t)(qb >> 16));
+            }
+            const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(g + 8 * m, (kx & 63) * 2));
+              mma_f16_16816(ui[pc & 1][m], a0, a1, a2, a3, xv.x, xv.y);
+            }
+          }
         } else if constexpr (FMT == FMT_INT8) {
 #pragma unroll
           for (int pc = 0; pc < 8; ++pc) {
@@ -488,6 +518,11 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
         for (int m = 0; m < MT; ++m)
 #pragma unroll
           for (int r = 0; r < 4; ++r) acci[m][r] += __float2int_rn(ui[0][m][r] + ui[1][m][r]);
+      } else if constexpr (kF8C) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[m][r] += ui[0][m][r] + ui[1][m][r];
       }
       // every shared-memory fragment of the unit has been read: hand the stage back
       __syncwarp();
