@@ -280,6 +280,10 @@ def mxfp4_act_quant(x_bits, w_packed, w_scale_bytes, rows=None, group=128):
 # ----------------------------------------------------------------------------------------
 # MoE: softmax top-k routing ([DSV4] §0.1 "M=1 MoE routing Q1"; the formula is the plain
 # softmax-then-top-k reading), then MXFP4 experts gate_up -> SiLU*mul -> down, weighted sum.
+# The clamped SwiGLU of [DSV4] §6.6 (J09, the SwiGLU fallback fix) and §9.4 (SwiGLU parameters
+# matching the model config, alpha = 1.0 and limit = 10.0) is the optional activation: the gate
+# is capped from above at limit, up is clipped to [-limit, limit], and the activation is
+# silu(alpha * gate) * up.  Without a limit (and alpha = 1) it is the plain SiLU*mul.
 # ----------------------------------------------------------------------------------------
 
 
@@ -315,9 +319,19 @@ def silu(g):
     return g / (1.0 + np.exp(-g))
 
 
-def moe_gate_up(x_bits, ids, w13, s13, I, pairs=None, cols=None):
+def swiglu(g, u, alpha=1.0, limit=None):
+    """silu(alpha * min(g, limit)) * clip(u, -limit, limit); limit None: no clamp."""
+    g = np.asarray(g, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    if limit is not None:
+        g = np.minimum(g, limit)
+        u = np.clip(u, -limit, limit)
+    return silu(alpha * g) * u
+
+
+def moe_gate_up(x_bits, ids, w13, s13, I, pairs=None, cols=None, alpha=1.0, limit=None):
     """Stage 1 for each (token m, slot j) pair: gu = W13[e] x_m with the dequantised expert,
-    g = gu[:I], u = gu[I:], h = bf16(silu(g) * u).
+    g = gu[:I], u = gu[I:], h = bf16(swiglu(g, u, alpha, limit)) (plain silu(g) * u by default).
 
     pairs: optional list of pair indices p = m*topk + j to evaluate (default all);
     cols:  optional intermediate indices i to evaluate (default all I).
@@ -341,7 +355,7 @@ def moe_gate_up(x_bits, ids, w13, s13, I, pairs=None, cols=None):
         n = cols.size
         out["g"][pi], out["u"][pi] = gu[:n], gu[n:]
         out["G"][pi], out["U"][pi] = au[:n], au[n:]
-    out["h_f64"] = silu(out["g"]) * out["u"]
+    out["h_f64"] = swiglu(out["g"], out["u"], alpha, limit)
     out["h"] = round_to_bf16(out["h_f64"])
     return out
 
@@ -367,9 +381,9 @@ def moe_down_combine(h_bits, ids, weights, w2, s2, rows=None):
     return round_to_bf16(y), y, a
 
 
-def moe_mxfp4(x_bits, logits_bits, w13, s13, w2, s2, I, topk, renormalize=False):
+def moe_mxfp4(x_bits, logits_bits, w13, s13, w2, s2, I, topk, renormalize=False, alpha=1.0, limit=None):
     """Whole MoE layer at a size the oracle finishes quickly (all pairs, all outputs)."""
     ids, w = route_topk(logits_bits, topk, renormalize)
-    st1 = moe_gate_up(x_bits, ids, w13, s13, I)
+    st1 = moe_gate_up(x_bits, ids, w13, s13, I, alpha=alpha, limit=limit)
     y, y64, a = moe_down_combine(st1["h"], ids, w, w2, s2)
     return {"ids": ids, "weights": w, "stage1": st1, "y": y, "y_f64": y64, "abs_sum": a}

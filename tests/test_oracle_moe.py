@@ -141,3 +141,66 @@ def test_planted_swapped_nibbles_caught(monkeypatch):
     monkeypatch.setattr(Q, "unpack_e2m1", swapped)
     with pytest.raises(AssertionError):
         test_mxfp4_dequant_exact_brute_force()
+
+
+# ------------------------------------------------------------------ clamped SwiGLU
+def test_swiglu_alpha_closed_form():
+    """sigmoid(ln 3) = 3/4, so silu(ln 3) = (3/4) ln 3.  With alpha = 2 and g = ln(3)/2 the
+    activation is (3/4) ln 3 * u; alpha outside the SiLU or dropped gives another number."""
+    g, u = np.log(3.0) / 2, 4.0
+    assert Q.swiglu(g, u, alpha=2.0, limit=10.0) == pytest.approx(0.75 * np.log(3.0) * 4.0, rel=1e-15)
+    assert Q.swiglu(np.log(3.0), u) == pytest.approx(3.0 * np.log(3.0), rel=1e-15)
+
+
+@pytest.mark.parametrize("alpha", [1.0, 1.702, 0.5])
+def test_swiglu_odd_part_is_alpha_g_u(alpha):
+    """silu(z) - silu(-z) = z (sigmoid(z) + sigmoid(-z) = 1): h(g) - h(-g) = alpha g u while
+    |g| stays inside the clamp."""
+    g = np.linspace(-9.5, 9.5, 39)
+    u = np.linspace(-7.0, 7.0, 39)
+    d = Q.swiglu(g, u, alpha, 10.0) - Q.swiglu(-g, u, alpha, 10.0)
+    assert np.allclose(d, alpha * g * u, rtol=1e-12, atol=1e-12)
+
+
+def test_swiglu_gate_capped_from_above_only():
+    u = np.array([3.0, -2.5, 0.75])
+    for g in (10.0, 10.5, 20.0, 1e6):  # at or above the limit the gate no longer matters
+        assert np.array_equal(Q.swiglu(g, u, 1.0, 10.0), Q.swiglu(10.0, u))
+    # no lower cap: a gate of -20 is used as it is, not raised to -10
+    assert np.array_equal(Q.swiglu(-20.0, u, 1.0, 10.0), Q.swiglu(-20.0, u))
+    assert not np.allclose(Q.swiglu(-20.0, u, 1.0, 10.0), Q.swiglu(-10.0, u))
+
+
+def test_swiglu_up_clipped_both_ways():
+    g = np.array([0.3, -1.0, 4.0])
+    assert np.array_equal(Q.swiglu(g, 25.0, 1.0, 10.0), Q.swiglu(g, 10.0))
+    assert np.array_equal(Q.swiglu(g, -25.0, 1.0, 10.0), Q.swiglu(g, -10.0))
+    assert np.array_equal(Q.swiglu(g, 9.0, 1.0, 10.0), Q.swiglu(g, 9.0))
+    # roles not swapped: gate -25 kept, up -25 clipped to -10
+    assert Q.swiglu(-25.0, -25.0, 1.0, 10.0) == Q.swiglu(-25.0, -10.0)
+
+
+def test_swiglu_no_limit_is_silu_mul():
+    rng = np.random.default_rng(3)
+    g, u = rng.normal(0, 8, 64), rng.normal(0, 8, 64)
+    assert np.array_equal(Q.swiglu(g, u), Q.silu(g) * u)
+    assert np.array_equal(Q.swiglu(g, u, 1.0, 1e300), Q.swiglu(g, u))
+
+
+def test_moe_gate_up_passes_the_clamp_through():
+    """Expert weights giving g = 12 (code 6.0 at scale 2^1) and u = 12 under limit 10 equal,
+    in the clamped stage, an expert giving g = u = 10 exactly (6 + 4) with no clamp."""
+    E, H, I = 1, 32, 32
+    x = synth.f32_to_bf16_bits(np.array([[1.0, 1.0] + [0.0] * (H - 2)], np.float32))
+    big = np.zeros((E, 2 * I, H // 2), np.uint8)
+    big[0, :, 0] = 0x07                          # k=0: 6.0, k=1: 0
+    s_big = np.full((E, 2 * I, 1), 128, np.uint8)  # 2^1
+    ten = np.zeros((E, 2 * I, H // 2), np.uint8)
+    ten[0, :, 0] = 0x67                          # k=0: 6.0 (low nibble), k=1: 4.0 (high nibble)
+    s_one = np.full((E, 2 * I, 1), 127, np.uint8)
+    ids = np.zeros((1, 1), np.int32)
+    a = Q.moe_gate_up(x, ids, big, s_big, I, limit=10.0)
+    b = Q.moe_gate_up(x, ids, ten, s_one, I)
+    assert np.all(a["g"] == 12.0) and np.all(b["g"] == 10.0)
+    assert np.array_equal(a["h"], b["h"])
+    assert not np.array_equal(Q.moe_gate_up(x, ids, big, s_big, I)["h"], b["h"])
