@@ -54,12 +54,14 @@ WORKLOADS = {
     "c3": "MXFP4 MoE decode: 256 experts, hidden 4096, intermediate 2048, top-8, M in 1..9",
     "c4": "tcgen05 block-scaled GEMM, 1x128 E4M3 activations, FP8 128x128 and MXFP4 weights, "
           "(N,K)=(17408,5120), M in {64,128,256}",
+    "n3": "MXFP4 MoE decode with clamped SwiGLU (alpha 1, limit 10): 256 experts, hidden 4096, "
+          "intermediate 2048, top-8, M in 1..9",
     "n2": "FP8 E4M3 per-channel-scaled decode GEMV, bf16 activations, (N,K) in "
           "{(17408,5120),(5120,17408),(10240,5120)} x M in {1,4,16}",
     "n4": "BF16 dense decode GEMV (unquantised weights), (N,K) in {(17408,5120),(5120,17408)} x M in {1,4,16}",
 }
 # the arithmetic type of each workload's weights
-DTYPES = {"c0": "int8", "c1": "int8", "c2": "fp8", "c3": "fp4", "c4": "fp8/fp4", "n2": "fp8", "n4": "bf16"}
+DTYPES = {"c0": "int8", "c1": "int8", "c2": "fp8", "c3": "fp4", "c4": "fp8/fp4", "n2": "fp8", "n3": "fp4", "n4": "bf16"}
 
 
 # ----------------------------------------------------------------------------- bytes / flops
@@ -246,7 +248,7 @@ def build_c2(ql, torch):
     return Workload("c2", calls, len(calls), cfg)
 
 
-def build_c3(ql, torch):
+def build_c3(ql, torch, limit=None, name="c3"):
     from oracle import qlinear_oracle as Q  # only to count the experts each routing touches
     E, H, I, topk = 256, 4096, 2048, 8
     w = synth.moe_weights_only(E, H, I, seed=0)
@@ -264,15 +266,20 @@ def build_c3(ql, torch):
         def call(sets=sets, y=y, state=state):
             x, lg, _ = sets[state["i"] % ROTATE]
             state["i"] += 1
-            ql.moe_mxfp4_grouped(x, *dev, router_logits=lg, topk=topk, out=y)
+            ql.moe_mxfp4_grouped(x, *dev, router_logits=lg, topk=topk, swiglu_limit=limit, out=y)
 
         uniq = float(np.mean([s[2] for s in sets]))
         b = uniq * bytes_moe_expert(H, I) + 2 * M * H * 2 + 2 * M * E
         calls.append({"fn": call, "M": M, "N": H, "K": I, "bytes": b, "flops": 2 * M * topk * 3 * H * I,
                       "x": sets[0][0], "y": y, "kind": "moe", "unique_experts": uniq})
-    cfg = {"workload": WORKLOADS["c3"],
+    cfg = {"workload": WORKLOADS[name],
            "bytes": "unique touched experts x 13369344 B + x + logits + y"}
-    return Workload("c3", calls, 4 * len(calls), cfg)
+    return Workload(name, calls, 3 * len(calls), cfg)  # gate_up (with routing), down, combine
+
+
+def build_n3(ql, torch):
+    """The MoE workload with the clamped SwiGLU (alpha 1, limit 10) as the expert activation."""
+    return build_c3(ql, torch, limit=10.0, name="n3")
 
 
 def build_c4(ql, torch):
@@ -374,14 +381,16 @@ def build_n2(ql, torch):
 
 
 BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4": build_c4, "n2": build_n2,
+            "n3": build_n3,
             "n4": build_n4}
 
 _SKINNY = ("skinny2_kernel (one launch per call: activation preparation + weight-streaming GEMM); "
            "achieved = algorithmic bytes per call / CUDA-event time per call (graphs of 32 back-to-back "
            "calls), aggregated over the step's calls")
+_MOE = ("MoE launches per call (gate_up with the routing fused in, down, combine); bytes of the touched "
+        "experts / event time per call")
 KERNEL_DESC = {"c0": _SKINNY, "c1": _SKINNY, "c2": _SKINNY, "n2": _SKINNY, "n4": _SKINNY,
-               "c3": "MoE launches per call (routing, gate_up, down, combine); bytes of the touched experts / "
-                     "event time per call",
+               "c3": _MOE, "n3": _MOE,
                "c4": "tcgen05 block-scaled GEMM + its activation-quantisation launch; bytes / event time per call"}
 
 
@@ -502,7 +511,7 @@ def oracle_sample(config, rows_per_call):
                 sec += time.perf_counter() - t
                 done += bytes_fp8(M, len(rows), K)
         desc = f"FP8 block oracle on the first {rows_per_call} output rows of each of the 8 calls"
-    elif config == "c3":
+    elif config in ("c3", "n3"):
         E, H, I = 256, 4096, 2048
         wsub = _case(("moe8",), lambda: synth.moe_weights_only(8, H, I, seed=0))
         for M in (1, 9):
@@ -511,7 +520,8 @@ def oracle_sample(config, rows_per_call):
             t = time.perf_counter()
             ids, _ = Q.route_topk(tk["logits"], 8)
             ids = np.asarray(ids) % 8  # 8 stand-in experts carry the sampled work
-            Q.moe_gate_up(tk["x"], ids, wsub["w13"], wsub["s13"], I, cols=cols)
+            Q.moe_gate_up(tk["x"], ids, wsub["w13"], wsub["s13"], I, cols=cols,
+                          limit=10.0 if config == "n3" else None)
             sec += time.perf_counter() - t
             done += len(np.unique(ids)) * 2 * len(cols) * (H // 2 + H // 32)
         desc = f"MoE oracle routing + gate_up on {rows_per_call} intermediate rows for M=1 and M=9"
@@ -630,7 +640,7 @@ def main():
 
     import torch
     if args.steps is None:
-        args.steps = {"c0": 20000, "c1": 4000, "c2": 4000, "c3": 2000, "c4": 2000, "n2": 3000,
+        args.steps = {"c0": 20000, "c1": 4000, "c2": 4000, "c3": 2000, "c4": 2000, "n2": 3000, "n3": 2000,
                       "n4": 2000}[args.config]
     torch.cuda.set_device(local)
     pg = None

@@ -228,13 +228,16 @@ QL_API ql_status qlinear_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t l
  *             topk_ids_in / topk_w_in and router_logits = NULL (exactly one of the two).
  *   dispatch: (token, slot) pairs grouped by expert, pairs of one expert in pair order.
  *   gate_up : for pair (m,j) with expert e: g = W13[e][0:I] x_m, u = W13[e][I:2I] x_m,
- *             h = bf16(silu(g) * u)
+ *             h = bf16( silu(alpha * min(g, limit)) * clamp(u, -limit, limit) )
+ *             (the clamped SwiGLU of [DSV4] §6.6 / §9.4, alpha = swiglu_alpha, limit =
+ *             swiglu_limit; limit = +infinity with alpha = 1 is the plain silu(g) * u)
  *   down    : y[m] = bf16( sum_j weight[m,j] * W2[e_(m,j)] h_(m,j) )
  * x: bf16 [M, H]; router_logits: bf16 [M, E]; topk_ids_in int32 [M, topk];
  * topk_w_in fp32 [M, topk]; w13: [E, 2I, H/2] packed E2M1, s13: [E, 2I, H/32] UE8M0;
  * w2: [E, H, I/2], s2: [E, H, I/32]; y: bf16 [M, H] (dense).
  * Debug outputs (nullable): topk_ids_out int32 [M, topk], topk_w_out fp32 [M, topk],
  * h_out bf16 [M*topk, I] (row m*topk + j).
+ * swiglu_alpha must be finite; swiglu_limit >= 0 (+infinity allowed), else QL_ERR_INVALID_ARG.
  * Requires 1 <= M <= 16, 1 <= topk <= min(E, 16), E <= 1024, H % 128 == 0, I % 128 == 0,
  * 16-byte aligned weight pointers.
  */
@@ -243,6 +246,7 @@ QL_API ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H,
                             const float* topk_w_in, int E, int topk, int renormalize,
                             const uint8_t* w13, const uint8_t* s13,
                             const uint8_t* w2, const uint8_t* s2, int64_t I,
+                            float swiglu_alpha, float swiglu_limit,
                             int32_t* topk_ids_out, float* topk_w_out, uint16_t* h_out,
                             uint16_t* y, void* workspace, size_t workspace_bytes,
                             ql_stream_t stream, int* path_out);

@@ -60,7 +60,7 @@ lib.qlinear_mxfp4.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64,
                               _vp, _vp, _vp, _sz, _vp, _ip]
 lib.moe_mxfp4_grouped.restype = _int
 lib.moe_mxfp4_grouped.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _int, _int, _int, _vp, _vp, _vp, _vp, _i64,
-                                  _vp, _vp, _vp, _vp, _vp, _sz, _vp, _ip]
+                                  ctypes.c_float, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _ip]
 
 OP_INT8_W8A8, OP_FP8_BLOCK, OP_MXFP4, OP_MOE_MXFP4, OP_BF16, OP_FP8_CHANNEL = 1, 2, 3, 4, 5, 6
 FP8_E4M3, FP8_E5M2 = 0, 1
@@ -247,10 +247,12 @@ def qlinear_fp8(x, w, w_scale, w_fmt="e4m3", bias=None, *, debug=False, out=None
 
 
 def moe_mxfp4_grouped(x, w13, s13, w2, s2, *, router_logits=None, topk_ids=None, topk_weights=None, topk=8,
-                      renormalize=False, debug=False, out=None, workspace=None, stream=None):
+                      renormalize=False, swiglu_alpha=1.0, swiglu_limit=None, debug=False, out=None, workspace=None,
+                      stream=None):
     """MXFP4 MoE decode layer.  x: bf16 [M, H]; w13 [E, 2I, H/2], s13 [E, 2I, H/32],
     w2 [E, H, I/2], s2 [E, H, I/32] (uint8).  Either router_logits (bf16 [M, E]) or
-    topk_ids/topk_weights.  debug=True returns (y, ids, weights, h, path)."""
+    topk_ids/topk_weights.  Expert activation silu(alpha * min(g, limit)) * clamp(u, +-limit)
+    (swiglu_limit None: plain silu(g) * u).  debug=True returns (y, ids, weights, h, path)."""
     _bf16(x, "x")
     M, H = x.shape
     E, twoI, _ = w13.shape
@@ -266,7 +268,8 @@ def moe_mxfp4_grouped(x, w13, s13, w2, s2, *, router_logits=None, topk_ids=None,
     ws = _ws(x.device, workspace_bytes(OP_MOE_MXFP4, M, H, I, E, topk), stream, workspace)
     path = ctypes.c_int(0)
     _check(lib.moe_mxfp4_grouped(_ptr(x), M, H, _ptr(router_logits), _ptr(topk_ids), _ptr(topk_weights), E, topk,
-                                 int(renormalize), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), I, _ptr(ids), _ptr(wts),
+                                 int(renormalize), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), I, float(swiglu_alpha),
+                                 float("inf") if swiglu_limit is None else float(swiglu_limit), _ptr(ids), _ptr(wts),
                                  _ptr(h), _ptr(y), _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(path)),
            "moe_mxfp4_grouped")
     if debug:

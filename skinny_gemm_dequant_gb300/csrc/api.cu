@@ -1,5 +1,6 @@
 // C ABI of the library (declared in include/qlinear.h): argument validation, workspace
 // layout, and the dispatch of each operation to its kernel sequence.
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 
@@ -596,10 +597,12 @@ ql_status qlinear_mxfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, co
 ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint16_t* router_logits,
                             const int32_t* topk_ids_in, const float* topk_w_in, int E, int topk, int renormalize,
                             const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, int64_t I,
-                            int32_t* topk_ids_out, float* topk_w_out, uint16_t* h_out, uint16_t* y,
-                            void* workspace, size_t workspace_bytes, ql_stream_t stream, int* path_out) {
+                            float swiglu_alpha, float swiglu_limit, int32_t* topk_ids_out, float* topk_w_out,
+                            uint16_t* h_out, uint16_t* y, void* workspace, size_t workspace_bytes,
+                            ql_stream_t stream, int* path_out) {
   if (path_out) *path_out = QL_PATH_NONE;
   if (!x || !w13 || !s13 || !w2 || !s2 || !y) return QL_ERR_INVALID_ARG;
+  if (!std::isfinite(swiglu_alpha) || std::isnan(swiglu_limit) || swiglu_limit < 0.f) return QL_ERR_INVALID_ARG;
   if ((router_logits == nullptr) == (topk_ids_in == nullptr)) return QL_ERR_INVALID_ARG;
   if (topk_ids_in && !topk_w_in) return QL_ERR_INVALID_ARG;
   if (M < 1 || H < 1 || I < 1 || E < 1 || topk < 1) return QL_ERR_INVALID_ARG;
@@ -643,6 +646,8 @@ ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint1
     a.I = (int)I;
     a.gu = at<float>(workspace, l.gus);
     a.slot_rows = l.slot_rows;
+    a.act_alpha = swiglu_alpha;
+    a.act_limit = swiglu_limit;
     a.M = (int)M;
     // stage 1: gate and up rows of W13[e] against every token's x
     a.N = (int)(2 * I);
@@ -655,7 +660,7 @@ ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint1
     a.s_estride = 2 * I * (H / 32);
     e = launch_moe2(S2_MOE_GU, l.gu, a, w13, H / 2, 2 * I * (H / 2), E, st);
     if (e != cudaSuccess) return cuda_status(e);
-    // stage 2: rows of W2[e] against the gathered h = bf16(silu(g) * u) of its pairs
+    // stage 2: rows of W2[e] against the gathered h = bf16(swiglu(g, u)) of its pairs
     a.N = (int)H;
     a.K = (int)I;
     a.x = nullptr;
@@ -704,6 +709,8 @@ ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint1
   a.I = (int)I;
   a.h = at<uint16_t>(workspace, l.h);
   a.h_dbg = h_out;
+  a.act_alpha = swiglu_alpha;
+  a.act_limit = swiglu_limit;
   a.o = at<float>(workspace, l.o);
   a.pdl = 1;
   // gate_up: rows 2I of W13[e], K = H, activations x[m]

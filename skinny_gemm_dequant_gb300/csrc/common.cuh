@@ -141,4 +141,10 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
+// the MoE expert activation: silu(alpha * min(g, limit)) * clamp(u, -limit, limit); limit =
+// +infinity and alpha = 1 give the plain silu(g) * u (fminf / fmaxf against infinity are exact)
+__device__ __forceinline__ float swiglu_f32(float g, float u, float alpha, float limit) {
+  return silu_f32(alpha * fminf(g, limit)) * fminf(fmaxf(u, -limit), limit);
+}
+
 }  // namespace ql

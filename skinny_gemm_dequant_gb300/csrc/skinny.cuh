@@ -65,6 +65,7 @@ struct SkinnyArgs {
   int topk, I;
   uint16_t* h;              // gate_up result [M*topk, I]
   uint16_t* h_dbg;          // optional copy
+  float act_alpha, act_limit;  // expert activation silu(alpha * min(g, limit)) * clamp(u, +-limit)
   float* o;                 // down result [M*topk, N]
   int pdl;
 };
@@ -505,7 +506,7 @@ __global__ void __launch_bounds__(SK_THREADS, 2) skinny_gemm_kernel(const __grid
           if (col < ntok && irow < a.I) {
             const float gv = res[m][i];
             const float uv = xch[(rw * 32 + lane) * 4 * MT + m * 4 + i];
-            const uint16_t hb = f32_to_bf16_rn(silu_f32(gv) * uv);
+            const uint16_t hb = f32_to_bf16_rn(swiglu_f32(gv, uv, a.act_alpha, a.act_limit));
             const int pr = s_pair[col];
             a.h[(int64_t)pr * a.I + irow] = hb;
             if (a.h_dbg) a.h_dbg[(int64_t)pr * a.I + irow] = hb;

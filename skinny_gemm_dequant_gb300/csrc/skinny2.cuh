@@ -97,6 +97,7 @@ struct Skinny2Args {
   float* gu;               // gate_up out / down in: [M*topk][2I] fp32 raw sums (gate rows, then up)
   int I;                   // expert intermediate size
   uint16_t* h_dbg;         // optional h = bf16(silu(g) * u) [M*topk][I]
+  float act_alpha, act_limit;  // expert activation silu(alpha * min(g, limit)) * clamp(u, +-limit)
   float* o;                // down out: [M*topk][H] fp32
   uint32_t* status;
   uint32_t wait_limit;
@@ -289,7 +290,8 @@ __device__ void s2_prepare(const Skinny2Args& a, int m, int sl, int nsl, int tid
 
 // MoE down activations, one job = (dispatch position q, slice sl of nsl).  The pair p = m*topk+j
 // at position q went to expert e; its gate and up sums g, u (length I) are gu[p].  Its activation
-// row is h = bf16(silu(g) * u) (the expert's intermediate, rounded to bf16 as the pages' BF16
+// row is h = bf16(silu(g) * u), or with a clamp bf16(silu(alpha min(g, limit)) clamp(u, +-limit))
+// (the expert's intermediate, rounded to bf16 as the pages' BF16
 // experts do), written as an f16 image row h * 2^-p (p from the row's amax, as for bf16 inputs)
 // at row rows[q] = slot(e) * slot_rows + (q - offsets[e]) of every copy (the routing wrote it);
 // slice 0 writes 2^p for the epilogue.  A pair beyond slot_rows of its expert (only possible when a token lists an expert
@@ -309,7 +311,7 @@ __device__ inline void s2_prepare_h(const Skinny2Args& a, int q, int sl, int nsl
     const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      hb[k] = f32_to_bf16_rn(silu_f32(gv[k]) * uv[k]);
+      hb[k] = f32_to_bf16_rn(swiglu_f32(gv[k], uv[k], a.act_alpha, a.act_limit));
       h[k] = bf16_bits_to_f32(hb[k]);
     }
   };

@@ -82,10 +82,13 @@ def test_moe_validation(lib):
     f = lib.moe_mxfp4_grouped
     f.restype = ctypes.c_int
     v, i64, c = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-    f.argtypes = [v, i64, i64, v, v, v, c, c, c, v, v, v, v, i64, v, v, v, v, v, ctypes.c_size_t, v,
+    fl = ctypes.c_float
+    f.argtypes = [v, i64, i64, v, v, v, c, c, c, v, v, v, v, i64, fl, fl, v, v, v, v, v, ctypes.c_size_t, v,
                   ctypes.POINTER(c)]
     path = c(0)
-    base = [16, 1, 256, 16, None, None, 16, 4, 0, 16, 16, 16, 16, 128, None, None, None, 16, 16, 1 << 30, None]
+    inf = float("inf")
+    base = [16, 1, 256, 16, None, None, 16, 4, 0, 16, 16, 16, 16, 128, 1.0, inf, None, None, None, 16, 16, 1 << 30,
+            None]
     args = list(base); args[3] = None                  # neither logits nor ids
     assert f(*args, ctypes.byref(path)) == 1
     args = list(base); args[1] = 17                    # M > 16
@@ -94,3 +97,6 @@ def test_moe_validation(lib):
     assert f(*args, ctypes.byref(path)) == 2
     args = list(base); args[13] = 100                  # I % 128
     assert f(*args, ctypes.byref(path)) == 2
+    for alpha, limit in ((float("nan"), 10.0), (inf, 10.0), (1.0, -1.0), (1.0, float("nan"))):
+        args = list(base); args[14], args[15] = alpha, limit   # SwiGLU alpha not finite / limit < 0 or NaN
+        assert f(*args, ctypes.byref(path)) == 1

@@ -36,17 +36,21 @@ def test_mxfp4_dense_bf16(ql, M, N, K):
 
 
 # ------------------------------------------------------------------ MoE
-def h_tolerance(st):
-    """|dh| <= 1e-3 (|silu'(g)| |u| G + |silu(g)| U) + 1.1e-6 G U + 2^-20 |h| + ulp(h):
-    the float bar on g and u (1e-3 * sum|w x|) carried through h = silu(g) * u, with
-    |silu'| <= 1.1, plus fp32 evaluation of silu and the final bf16 rounding."""
+def h_tolerance(st, alpha=1.0, limit=None):
+    """|dh| <= 1e-3 (1.1 alpha |u_c| G + |silu(alpha g_c)| U) + 1.1e-6 alpha G U + 2^-20 |h|
+    + ulp(h): the float bar on g and u (1e-3 * sum|w x|) carried through
+    h = silu(alpha g_c) * u_c, where g_c = min(g, limit) and u_c = clip(u, +-limit) are
+    1-Lipschitz in g and u and |d silu(alpha g)/dg| <= 1.1 alpha, plus fp32 evaluation of
+    the activation and the final bf16 rounding."""
     g, u, G, U = st["g"], st["u"], st["G"], st["U"]
-    s = g / (1 + np.exp(-g))
-    return 1e-3 * (1.1 * np.abs(u) * G + np.abs(s) * U) + 1.1e-6 * G * U + 2.0 ** -20 * np.abs(s * u) \
-        + F.bf16_ulp(st["h_f64"])
+    if limit is not None:
+        g, u = np.minimum(g, limit), np.clip(u, -limit, limit)
+    s = Q.silu(alpha * g)
+    return 1e-3 * (1.1 * abs(alpha) * np.abs(u) * G + np.abs(s) * U) + 1.1e-6 * abs(alpha) * G * U \
+        + 2.0 ** -20 * np.abs(s * u) + F.bf16_ulp(st["h_f64"])
 
 
-def run_moe(ql, c, wdev, topk, ids=None, wts=None):
+def run_moe(ql, c, wdev, topk, ids=None, wts=None, alpha=1.0, limit=None):
     x = to_bf16_tensor(c["x"])
     kw = {}
     if ids is None:
@@ -54,13 +58,14 @@ def run_moe(ql, c, wdev, topk, ids=None, wts=None):
     else:
         kw["topk_ids"] = torch.from_numpy(ids).cuda()
         kw["topk_weights"] = torch.from_numpy(wts).cuda()
-    y, gi, gw, h, path = ql.moe_mxfp4_grouped(x, *wdev, topk=topk, debug=True, **kw)
+    y, gi, gw, h, path = ql.moe_mxfp4_grouped(x, *wdev, topk=topk, swiglu_alpha=alpha, swiglu_limit=limit,
+                                              debug=True, **kw)
     torch.cuda.synchronize()
     assert path == "moe_mxfp4"
     return bits_of(y), gi.cpu().numpy(), gw.cpu().numpy(), bits_of(h)
 
 
-def check_moe(c, got, I, topk, cols=None, rows=None, ids=None, wts=None):
+def check_moe(c, got, I, topk, cols=None, rows=None, ids=None, wts=None, alpha=1.0, limit=None):
     y, gi, gw, h = got
     if ids is None:
         ids, wts = Q.route_topk(c["logits"], topk)
@@ -68,15 +73,16 @@ def check_moe(c, got, I, topk, cols=None, rows=None, ids=None, wts=None):
         assert np.allclose(gw, wts, rtol=1e-6, atol=0), "routing weights differ"
     M = c["x"].shape[0]
     cols = np.arange(I) if cols is None else cols
-    st = Q.moe_gate_up(c["x"], ids, c["w13"], c["s13"], I, cols=cols)
+    st = Q.moe_gate_up(c["x"], ids, c["w13"], c["s13"], I, cols=cols, alpha=alpha, limit=limit)
     hv = F.bf16_to_f64(h[:, cols])
     err = np.abs(hv - F.bf16_to_f64(st["h"]))
-    tol = h_tolerance(st)
+    tol = h_tolerance(st, alpha, limit)
     assert np.all(err <= tol), f"h: {np.sum(err > tol)} entries outside tolerance"
     # stage 2 on the kernel's own h: y within 1e-3 * sum_j |w_j| sum_i |W2 h| + 1 ulp
     yb, y64, a = Q.moe_down_combine(h, ids, np.asarray(gw, np.float64), c["w2"], c["s2"], rows=rows)
     sl = slice(None) if rows is None else rows
     check_float(y[:, sl], y64, a)
+    return st
 
 
 @pytest.mark.parametrize("M", [1, 3, 9, 16])
@@ -149,3 +155,50 @@ def test_moe_full_size_sampled(ql, moe_full, M):
     c = dict(w, **synth.moe_tokens(M, E, H, seed=0))
     got = run_moe(ql, c, dev, topk)
     check_moe(c, got, I, topk, cols=sample_rows(I, 24, seed=M), rows=sample_rows(H, 24, seed=M + 1))
+
+
+# ------------------------------------------------------------------ clamped SwiGLU
+def _clamps_exercised(st, limit):
+    """the case really clamps: some gates above the limit, some ups beyond it on each side"""
+    g, u = st["g"], st["u"]
+    assert np.any(g > limit) and np.any(u > limit) and np.any(u < -limit)
+
+
+@pytest.mark.parametrize("alpha,limit", [(1.0, 10.0), (1.702, 7.0)])
+@pytest.mark.parametrize("M", [1, 9])
+def test_moe_swiglu_clamp_persistent_kernel(ql, M, alpha, limit):
+    E, H, I, topk = 16, 512, 256, 4
+    c = synth.moe_case(M, E, H, I, seed=60 + M)
+    wdev = [torch.from_numpy(c[k]).cuda() for k in ("w13", "s13", "w2", "s2")]
+    st = check_moe(c, run_moe(ql, c, wdev, topk, alpha=alpha, limit=limit), I, topk, alpha=alpha, limit=limit)
+    _clamps_exercised(st, limit)
+
+
+@pytest.mark.parametrize("M", [2, 16])
+def test_moe_swiglu_clamp_register_kernel(ql, M):
+    # I = 128: not a whole 256-K unit, so the MoE runs on the register kernel path
+    E, H, I, topk = 16, 256, 128, 4
+    c = synth.moe_case(M, E, H, I, seed=70 + M)
+    wdev = [torch.from_numpy(c[k]).cuda() for k in ("w13", "s13", "w2", "s2")]
+    st = check_moe(c, run_moe(ql, c, wdev, topk, alpha=1.0, limit=3.0), I, topk, alpha=1.0, limit=3.0)
+    _clamps_exercised(st, 3.0)
+
+
+def test_moe_swiglu_rejects_bad_parameters(ql):
+    E, H, I, topk = 8, 256, 256, 2
+    c = synth.moe_case(1, E, H, I, seed=5)
+    wdev = [torch.from_numpy(c[k]).cuda() for k in ("w13", "s13", "w2", "s2")]
+    for alpha, limit in ((float("nan"), 10.0), (1.0, -1.0), (1.0, float("nan")), (float("inf"), 10.0)):
+        with pytest.raises(ql.QLError):
+            run_moe(ql, c, wdev, topk, alpha=alpha, limit=limit)
+
+
+@pytest.mark.parametrize("M", [1, 9])
+def test_moe_swiglu_clamp_full_size_sampled(ql, moe_full, M):
+    E, H, I, topk = 256, 4096, 2048, 8
+    w, dev = moe_full
+    c = dict(w, **synth.moe_tokens(M, E, H, seed=3))
+    got = run_moe(ql, c, dev, topk, alpha=1.0, limit=10.0)
+    st = check_moe(c, got, I, topk, cols=sample_rows(I, 48, seed=M), rows=sample_rows(H, 24, seed=M + 1),
+                   alpha=1.0, limit=10.0)
+    _clamps_exercised(st, 10.0)
