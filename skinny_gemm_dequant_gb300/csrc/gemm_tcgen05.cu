@@ -51,7 +51,19 @@ struct TcParams {
   uint32_t* status;
   uint32_t wait_limit;
   int sf_layout;  // 0: row r at (lane r % 32 of every quadrant, column r / 32); 1: (lane r, column 0)
+  int staged;     // 1: every scale byte of the CTA is copied to shared memory once, at the start
+  uint32_t sc_w_bytes;  // shared-memory bytes of the staged weight scales (16-byte multiple)
 };
+
+// Staged scales, behind the mbarriers:
+//   weights, FP8: one byte per stage (the CTA's 128 rows share one 128x128 block row);
+//   weights, FP4: one 32-bit word (4 x 32-K scale bytes) per row and stage, stage-major, the row
+//                 index XORed with (stage & 31) so that both the staging writes (consecutive
+//                 stages) and the per-stage reads (consecutive rows) hit 32 distinct banks;
+//   activations: one byte per token of the tile and stage, stage-major.
+__host__ __device__ constexpr uint32_t sc_w_bytes(int fp4, int nk) {
+  return ((uint32_t)(fp4 ? nk * 128 * 4 : nk) + 15u) & ~15u;
+}
 
 __device__ __forceinline__ uint32_t rep4(uint32_t b) { return (b & 0xFFu) * 0x01010101u; }
 
@@ -73,6 +85,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* sf_full = bars + S;
   uint64_t* empty = bars + 2 * S;
   uint64_t* acc_full = bars + 3 * S;
+  uint8_t* sc_w = reinterpret_cast<uint8_t*>(bars + 3 * S + 2);  // staged scales (p.staged)
+  uint8_t* sc_a = sc_w + p.sc_w_bytes;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -138,7 +152,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread issues every MMA, so the loop body is kept to the MMAs themselves: instruction
+    // descriptors are built once, and shared-memory descriptors (linear in the address: the
+    // start-address field holds address / 16) advance by constants
     const uint32_t a_fmt = p.fp4 ? 5u : 0u;  // E2M1 or E4M3
+    uint32_t idesc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) idesc[j] = idesc_mxf8f6f4(a_fmt, 0u, (uint32_t)p.sub_n, (uint32_t)j, (uint32_t)j);
+    const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA)), b_desc0 = smem_desc_sw128(smem_u32(sB));
+    const uint32_t a_step = a_bytes >> 4, b_step = b_bytes >> 4, b_sub = ((uint32_t)p.sub_n * kBlockK) >> 4;
+    const uint32_t sf_stride = 4 + 4 * (uint32_t)p.nsub;
+    const bool two = p.nsub > 1;
     for (int kt = 0; kt < nk; ++kt) {
       const int s = kt % S;
       const uint32_t par = (uint32_t)(kt / S) & 1;
@@ -147,46 +171,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t a_base = smem_u32(sA + (size_t)s * a_bytes);
-      const uint32_t b_base = smem_u32(sB + (size_t)s * b_bytes);
-      const uint32_t sf_col = kSfCol0 + (uint32_t)s * (4 + 4 * p.nsub);
+      const uint64_t ad = a_desc0 + (uint64_t)((uint32_t)s * a_step), bd = b_desc0 + (uint64_t)((uint32_t)s * b_step);
+      const uint32_t sfa = tmem + kSfCol0 + (uint32_t)s * sf_stride;
+      // four 32-K steps (32 bytes = 2 descriptor units each), scale byte j of each vector
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {  // four 32-K steps, scale byte j of each vector
-        for (int sub = 0; sub < p.nsub; ++sub) {
-          const uint32_t idesc = idesc_mxf8f6f4(a_fmt, 0u, (uint32_t)p.sub_n, (uint32_t)j, (uint32_t)j);
-          const uint64_t ad = smem_desc_sw128(a_base + 32 * j);
-          const uint64_t bd = smem_desc_sw128(b_base + (uint32_t)sub * p.sub_n * kBlockK + 32 * j);
-          mma_mxf8f6f4(tmem + (uint32_t)sub * p.sub_n, ad, bd, idesc, tmem + sf_col, tmem + sf_col + 4 + 4 * sub,
+      for (int j = 0; j < 4; ++j) {
+        mma_mxf8f6f4(tmem, ad + 2 * j, bd + 2 * j, idesc[j], sfa, sfa + 4, (kt > 0 || j > 0) ? 1u : 0u);
+        if (two)
+          mma_mxf8f6f4(tmem + (uint32_t)p.sub_n, ad + 2 * j, bd + b_sub + 2 * j, idesc[j], sfa, sfa + 8,
                        (kt > 0 || j > 0) ? 1u : 0u);
-        }
       }
       tc_commit(&empty[s]);
     }
     tc_commit(acc_full);  // completes once every MMA issued above has finished
     if (*abort) mbar_wait(acc_full, 0, kDrainLimit, nullptr);
-  } else if (warp >= 4) {
+  } else if (warp >= 2) {
     // ------------------------------------------------------------ scale vectors, then epilogue
+    pdl_wait();  // activation scales come from the quantisation kernel
+    if (p.staged) {
+      // warps 2..7 copy the CTA's scale bytes to shared memory once; out-of-range rows and
+      // tokens get the neutral scale 2^0
+      const int tid = threadIdx.x - 64, nthr = kThreads - 64;
+      if (p.fp4) {
+        uint32_t* w32 = reinterpret_cast<uint32_t*>(sc_w);
+        for (int i = tid; i < 128 * nk; i += nthr) {
+          const int r = i / nk, kt = i - r * nk;  // consecutive threads: consecutive stages of a row
+          const int n = n0 + r;
+          const uint32_t v =
+              n < p.N ? __ldg(reinterpret_cast<const uint32_t*>(p.ws + (int64_t)n * p.lds + 4 * kt)) : 0x7F7F7F7Fu;
+          w32[kt * 128 + (r ^ (kt & 31))] = v;
+        }
+      } else {
+        for (int kt = tid; kt < nk; kt += nthr) sc_w[kt] = n0 < p.N ? __ldg(p.ws + (int64_t)(n0 / 128) * p.lds + kt) : 0x7F;
+      }
+      for (int i = tid; i < p.tt * nk; i += nthr) {
+        const int kt = i / p.tt, t = i - kt * p.tt;  // consecutive threads: consecutive tokens
+        sc_a[i] = t0 + t < p.M ? __ldg(p.as + (int64_t)(t0 + t) * p.las + kt) : 0x7F;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 64) : "memory");
+    }
+  }
+  if (warp >= 4) {
     const int q = warp - 4;  // tensor-memory lane quadrant of this warp
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    pdl_wait();
     bool ok = true;
-    for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % S;
-      const uint32_t it = kt / S;
-      // lane 0 waits and the result is broadcast, so the warp stays converged for the
-      // .sync.aligned tensor-memory stores below
-      int got = 0;
-      if (lane == 0) got = mbar_wait(&empty[s], (it - 1) & 1, lim, abort);
-      got = __shfl_sync(0xffffffffu, got, 0);
-      if (!got) {
-        if (lane == 0) fail();
-        ok = false;
-        break;
+    // the scale words of a stage are read kPD stages ahead into registers (the loop is unrolled
+    // by kPD so every array index is a constant).  Staged, they come from shared memory; else
+    // from global memory, and then every stage also waits for an L2 round trip, because the
+    // release of the mbarrier arrive waits for the loads issued before it
+    constexpr int kPD = 4;
+    uint32_t pw[kPD][4], pb[kPD][2][4];
+    auto fetch = [&](int kt, uint32_t (&wa)[4], uint32_t (&wb)[2][4]) {
+      if (kt >= nk) return;
+      if (p.staged) {  // shared memory: no global load (and no wait for one) inside the loop
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = (p.sf_layout == 0) ? (lane + 32 * j) : (32 * q + lane);
+          wa[j] = p.fp4 ? reinterpret_cast<const uint32_t*>(sc_w)[kt * 128 + (r ^ (kt & 31))] : rep4(sc_w[kt]);
+        }
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = (p.sf_layout == 0) ? (lane + 32 * j) : (32 * q + lane);
+            wb[sub][j] = (sub < p.nsub && r < p.sub_n) ? rep4(sc_a[kt * p.tt + sub * p.sub_n + r]) : 0x7F7F7F7Fu;
+          }
+        return;
       }
-      tc_fence_after();
-      const uint32_t sf_col = kSfCol0 + (uint32_t)s * (4 + 4 * p.nsub);
-      // weight scale vectors: one byte per 32-K step (4 per stage) for each of the 128 rows
-      uint32_t wa[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int r = (p.sf_layout == 0) ? (lane + 32 * j) : (32 * q + lane);
@@ -198,22 +249,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         wa[j] = wv;
       }
-      tmem_st_x4(tmem + lane_base + sf_col, wa[0], wa[1], wa[2], wa[3]);
-      // activation scale vectors: the token's 1x128 scale repeated for the 4 steps
-      for (int sub = 0; sub < p.nsub; ++sub) {
-        uint32_t wb[4];
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int r = (p.sf_layout == 0) ? (lane + 32 * j) : (32 * q + lane);
           const int t = t0 + sub * p.sub_n + r;
-          wb[j] = (r < p.sub_n && t < p.M) ? rep4(__ldg(p.as + (int64_t)t * p.las + kt)) : 0x7F7F7F7Fu;
+          wb[sub][j] = (sub < p.nsub && r < p.sub_n && t < p.M) ? rep4(__ldg(p.as + (int64_t)t * p.las + kt))
+                                                                : 0x7F7F7F7Fu;
         }
-        tmem_st_x4(tmem + lane_base + sf_col + 4 + 4 * sub, wb[0], wb[1], wb[2], wb[3]);
+    };
+#pragma unroll
+    for (int d = 0; d < kPD; ++d) fetch(d, pw[d], pb[d]);
+    for (int k0 = 0; k0 < nk && ok; k0 += kPD) {
+#pragma unroll
+      for (int d = 0; d < kPD; ++d) {
+        const int kt = k0 + d;
+        if (kt >= nk) break;
+        const int s = kt % S;
+        const uint32_t it = kt / S;
+        // lane 0 waits and the result is broadcast, so the warp stays converged for the
+        // .sync.aligned tensor-memory stores below
+        int got = 0;
+        if (lane == 0) got = mbar_wait(&empty[s], (it - 1) & 1, lim, abort);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          if (lane == 0) fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sf_col = kSfCol0 + (uint32_t)s * (4 + 4 * p.nsub);
+        // weight scale vectors: one byte per 32-K step (4 per stage) for each of the 128 rows;
+        // then the activation scale vectors: the token's 1x128 scale repeated for the 4 steps
+        tmem_st_x4(tmem + lane_base + sf_col, pw[d][0], pw[d][1], pw[d][2], pw[d][3]);
+        tmem_st_x4(tmem + lane_base + sf_col + 4, pb[d][0][0], pb[d][0][1], pb[d][0][2], pb[d][0][3]);
+        if (p.nsub > 1) tmem_st_x4(tmem + lane_base + sf_col + 8, pb[d][1][0], pb[d][1][1], pb[d][1][2], pb[d][1][3]);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_full[s]);
+        fetch(kt + kPD, pw[d], pb[d]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sf_full[s]);
     }
     int got = 0;
     if (ok && lane == 0) got = mbar_wait(acc_full, 0, lim, abort);
@@ -301,7 +378,13 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   p.tt = p.nsub * p.sub_n;
   const size_t stage = (size_t)kBlockN * kBlockK + (size_t)p.tt * kBlockK;
   const size_t budget = 227 * 1024 - 1024 - 256;
-  int S = (int)(budget / stage);
+  const int nk = g.K / kBlockK;
+  // stage the scales in shared memory when they take at most 48 KB and leave two stages
+  const size_t sc_bytes = sc_w_bytes(g.fp4, nk) + (((size_t)p.tt * nk + 15) & ~(size_t)15);
+  p.staged = (sc_bytes <= 48 * 1024 && budget >= sc_bytes + 2 * stage) ? 1 : 0;
+  p.sc_w_bytes = p.staged ? sc_w_bytes(g.fp4, nk) : 0;
+  const size_t extra = p.staged ? sc_bytes : 0;
+  int S = (int)((budget - extra) / stage);
   if (S > 8) S = 8;
   p.stages = S;
   p.ws = g.ws;
@@ -324,7 +407,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
                              kBlockK, (uint32_t)p.tt);
   if (!ok_a || !ok_b) return cudaErrorInvalidValue;
 
-  const size_t smem = 1024 + (size_t)S * stage + (size_t)(3 * S + 1) * 8;
+  const size_t smem = 1024 + (size_t)S * stage + (size_t)(3 * S + 2) * 8 + extra;
   static std::atomic<int> attr_set{0};
   if (!attr_set.load()) {
     cudaError_t e = raise_smem_limit(tc_gemm_kernel);

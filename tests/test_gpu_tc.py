@@ -82,3 +82,25 @@ def test_tc_mxfp4_full_size_sampled(ql, M):
     r = Q.mxfp4_act_quant(c["x"], c["w"], c["s"], rows=rows)
     assert np.array_equal(aq, r["q"]) and np.array_equal(as_, r["s"])
     check_float(y[:, rows], r["y_f64"], r["abs_sum"])
+
+
+# Long K: the scales of (256, 256, 32768) and of both MXFP4 cases do not fit the 48 KB
+# shared-memory staging area, so the kernel reads them from global memory stage by stage;
+# (64, 130, 40960) still stages them (320 stages of scales)
+@pytest.mark.parametrize("M,N,K", [(256, 256, 32768), (64, 130, 40960)])
+def test_tc_fp8_long_k(ql, M, N, K):
+    c = synth.fp8_block_case(M, N, K, seed=7)
+    y, aq, as_ = run_fp8(ql, c, K)
+    r = Q.fp8_block_act_quant(c["x"], c["w"], c["s"], K)
+    assert np.array_equal(aq, r["q"]) and np.array_equal(as_, r["s"])
+    check_float(y, r["y_f64"], r["abs_sum"])
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 256, 32768), (200, 128, 16384)])
+def test_tc_mxfp4_long_k(ql, M, N, K):
+    c0 = synth.mxfp4_dense_case(M, N, K, seed=8)
+    c, s_raw = pad_scales(c0, K)
+    y, aq, as_ = run_fp4(ql, c)
+    r = Q.mxfp4_act_quant(c0["x"], c0["w"], s_raw)
+    assert np.array_equal(aq, r["q"]) and np.array_equal(as_, r["s"])
+    check_float(y, r["y_f64"], r["abs_sum"])
