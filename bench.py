@@ -100,8 +100,8 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha1()
-    for f in ("skinny2.cuh", "kernels_skinny2.cu", "skinny.cuh", "kernels_skinny.cu", "kernels_quant.cu",
-              "kernels_moe.cu", "gemm_tcgen05.cu", "tc_ptx.cuh", "common.cuh"):
+    for f in ("skinny2.cuh", "skinny2_kernel.cuh", "kernels_skinny2.cu", "skinny.cuh", "kernels_skinny.cu",
+              "kernels_quant.cu", "kernels_moe.cu", "gemm_tcgen05.cu", "tc_ptx.cuh", "common.cuh", "api.cu"):
         h.update(open(os.path.join(ROOT, "skinny_gemm_dequant_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:12]
 
