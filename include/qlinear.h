@@ -82,7 +82,8 @@ enum {
   QL_PATH_MXFP4_TCGEN05 = 5,   /* 1x128 act quant + tcgen05 block-scaled GEMM (E4M3 x E2M1) */
   QL_PATH_MOE_MXFP4 = 6,       /* routing + dispatch + gate_up/SiLU + down + combine         */
   QL_PATH_BF16_SKINNY = 7,     /* BF16 skinny GEMM (unquantised weights)                    */
-  QL_PATH_FP8_CHANNEL_SKINNY = 8 /* FP8 skinny GEMM, per-channel / per-tensor fp32 scale     */
+  QL_PATH_FP8_CHANNEL_SKINNY = 8, /* FP8 skinny GEMM, per-channel / per-tensor fp32 scale    */
+  QL_PATH_INT8_TCGEN05 = 9       /* per-token INT8 quant + tcgen05 GEMM on exact f16 images  */
 };
 
 /* device status flags (bitmask) */
@@ -123,11 +124,14 @@ QL_API void ql_set_wait_limit(uint32_t polls);
  *   x_q[m,k]= clamp(round_half_even(x[m,k] / x_s[m]), -127, 127)   (0 if x_s == 0)
  *   acc[m,n]= sum_k x_q[m,k] * w[n,k]                    (exact int32)
  *   y[m,n]  = bf16((acc * x_s[m]) * w_s[n])  then, if bias, y = bf16(y + bias[n])
- * x: bf16 [M, ldx] (K used); w: int8 [N, ldw], K-contiguous, "not transposed, not
- * dequantised"; w_scale: fp32 [N] (per channel) or [1] (per tensor, w_scale_len == 1);
+ * x: bf16 [M, ldx] (K used); w: int8 [N, ldw], K-contiguous, used as stored (no transpose,
+ * no dequantised copy); w_scale: fp32 [N] (per channel) or [1] (per tensor, w_scale_len == 1);
  * bias: nullable bf16 [N]; y: bf16 [M, ldy].
  * Debug outputs (nullable): acc_out int32 [M, N] (dense, ld N), xq_out int8 [M, K] (ld K),
  * xs_out fp32 [M].
+ * Paths: M <= 16 -> the persistent skinny kernel (quantisation fused in, one launch);
+ *        M > 16  -> a quantisation launch + the tcgen05 GEMM (kind::f16 MMAs on the exact f16
+ *                   values of the codes and weights, drained to int32 every 512 K).
  * Requires: M >= 1, N >= 1, K >= 16, K % 16 == 0, ldx >= K, ldw >= K, ldw % 16 == 0,
  * ldy >= N, 16-byte aligned x and w, |acc| < 2^31 (always true for K <= 133152).
  */

@@ -4,6 +4,7 @@
 #include <cstdio>
 #include <cstring>
 
+#include "gemm_i8_tcgen05.h"
 #include "gemm_tcgen05.h"
 #include "internal.h"
 #include "skinny2.cuh"
@@ -196,6 +197,19 @@ MoeLayout moe_layout(int64_t M, int64_t H, int64_t I, int E, int topk) {
   return l;
 }
 
+// workspace of the INT8 tcgen05 GEMM (M > 16): f16 activation codes and per-token scales
+struct I8Layout {
+  size_t img, xs, total;
+};
+I8Layout i8_layout(int64_t M, int64_t K) {
+  I8Layout l;
+  Carver c;
+  l.img = c.take(tc::i8_image_bytes(M, K));
+  l.xs = c.take((size_t)M * 4);
+  l.total = c.off;
+  return l;
+}
+
 // workspace for the tcgen05 path (activation codes and scales) plus the skinny fallbacks
 size_t act_quant_ws(int64_t M, int64_t K) {
   Carver c;
@@ -272,8 +286,11 @@ size_t ql_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int to
   if (M < 0 || N < 0 || K < 0) return 0;
   const int64_t Mc = M < 16 ? M : 16;  // skinny kernels run 16 tokens at a time
   switch (op) {
-    case QL_OP_INT8_W8A8:
-      return dense2_layout(FMT_INT8, Mc, N, K, 128).total;
+    case QL_OP_INT8_W8A8: {
+      const size_t a = dense2_layout(FMT_INT8, Mc, N, K, 128).total;
+      const size_t b = M > 16 ? i8_layout(M, K).total : 0;
+      return a > b ? a : b;
+    }
     case QL_OP_FP8_BLOCK: {
       // block_n is not known here: 16 (the smallest accepted) bounds the scale staging
       size_t a = dense2_layout(FMT_FP8, Mc, N, K, 16).total;
@@ -334,6 +351,35 @@ ql_status qlinear_int8_w8a8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
   if (!workspace || workspace_bytes < ql_workspace_bytes(QL_OP_INT8_W8A8, M, N, K, 0, 0)) return QL_ERR_WORKSPACE;
   if (!al16(workspace)) return QL_ERR_ALIGNMENT;
   cudaStream_t st = (cudaStream_t)stream;
+
+  if (M > 16) {
+    // prefill-sized batches: one GEMM on the tensor cores streams the weights once
+    const I8Layout l = i8_layout(M, K);
+    tc::I8GemmArgs g = {};
+    g.M = (int)M;
+    g.N = (int)N;
+    g.K = (int)K;
+    g.x = x;
+    g.ldx = ldx;
+    g.w = w;
+    g.ldw = ldw;
+    g.w_s = w_scale;
+    g.w_s_len = (int)w_scale_len;
+    g.bias = bias;
+    g.y = y;
+    g.ldy = ldy;
+    g.acc_out = acc_out;
+    g.xq_dbg = xq_out;
+    g.xs_dbg = xs_out;
+    g.img = at<uint16_t>(workspace, l.img);
+    g.xs = at<float>(workspace, l.xs);
+    g.status = at<uint32_t>(workspace, 0);
+    g.wait_limit = g_wait_limit;
+    const cudaError_t e = tc::launch_i8_gemm(g, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (path_out) *path_out = QL_PATH_INT8_TCGEN05;
+    return QL_OK;
+  }
 
   Dense2Call d = {};
   d.fmt = FMT_INT8;

@@ -23,7 +23,8 @@ def run(ql, c, bias=None, wsl=None):
     b = None if bias is None else to_bf16_tensor(bias)
     y, acc, xq, xs, path = ql.qlinear_int8_w8a8(x, w, ws, b, debug=True)
     torch.cuda.synchronize()
-    assert path == "int8_skinny"
+    # up to 16 tokens: the persistent skinny kernel; more: the tcgen05 GEMM
+    assert path == ("int8_skinny" if c["x"].shape[0] <= 16 else "int8_tcgen05")
     return bits_of(y), acc.cpu().numpy(), xq.cpu().numpy(), xs.cpu().numpy()
 
 
@@ -78,5 +79,52 @@ def test_int8_repeat_is_deterministic(ql):
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
 def test_int8_full_size_sampled(ql, N, K, M):
     c = synth.int8_case(M, N, K, seed=0)
+    rows = sample_rows(N, seed=M)
+    compare(c, run(ql, c), rows=rows)
+
+
+# ------------------------------------------------------------------ M > 16: the tcgen05 GEMM
+@pytest.mark.parametrize("M,N,K", [(17, 128, 256), (33, 200, 320), (64, 256, 1024), (100, 300, 640),
+                                   (128, 130, 2048), (129, 64, 512), (200, 384, 1088), (256, 512, 4096)])
+def test_int8_gemm_small_and_ragged(ql, M, N, K):
+    c = synth.int8_case(M, N, K, seed=M + N + K)
+    compare(c, run(ql, c))
+
+
+def test_int8_gemm_bias_per_tensor_scale_padded_rows(ql):
+    c = synth.int8_case(40, 150, 576, seed=21, ldw=640)
+    bias = synth.bf16_normal(synth.rng(21, 99), (150,))
+    compare(c, run(ql, c, bias=bias, wsl=1), bias=bias, wsl=1)
+
+
+@pytest.mark.parametrize("sign", ["same", "mixed"])
+def test_int8_gemm_drain_exactness_at_the_limit(ql, sign):
+    # every code and weight at +-127: each 512-K group sums to 512 * 127^2 = 8,258,048 (just below
+    # 2^23) and the whole K to 16384 * 127^2 = 264,257,536, exact only through the int32 drain
+    M, N, K = 24, 130, 16384
+    c = synth.int8_case(M, N, K, seed=22)
+    c["x"][:] = synth.f32_to_bf16_bits(np.full((M, K), 2.0, np.float32))
+    c["w"][:] = 127
+    if sign == "mixed":
+        c["x"][1::2, ::3] = synth.f32_to_bf16_bits(np.float32(-2.0))
+        c["w"][::2, 1::2] = -127
+    got = run(ql, c)
+    assert got[1].max() == K * 127 * 127 or sign == "mixed"
+    compare(c, got)
+
+
+def test_int8_gemm_zero_token_and_large_values(ql):
+    c = synth.int8_case(20, 128, 256, seed=23)
+    c["x"][1] = 0
+    c["x"][19] = synth.f32_to_bf16_bits(np.linspace(-3e4, 3e4, 256).astype(np.float32))
+    got = run(ql, c)
+    assert got[3][1] == 0 and not got[2][1].any() and not got[0][1].any()
+    compare(c, got)
+
+
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408), (10240, 5120)])
+@pytest.mark.parametrize("M", [32, 256])
+def test_int8_gemm_full_size_sampled(ql, N, K, M):
+    c = synth.int8_case(M, N, K, seed=1)
     rows = sample_rows(N, seed=M)
     compare(c, run(ql, c), rows=rows)
