@@ -56,12 +56,14 @@ WORKLOADS = {
           "(N,K)=(17408,5120), M in {64,128,256}",
     "n3": "MXFP4 MoE decode with clamped SwiGLU (alpha 1, limit 10): 256 experts, hidden 4096, "
           "intermediate 2048, top-8, M in 1..9",
+    "n1": "INT8 W8A8 GEMM on the tcgen05 path (per-token quantisation + kind::f16 MMAs on exact f16 images), "
+          "27B-class shapes (N,K) in {(17408,5120),(5120,17408),(10240,5120)} x M in {32,64,128,256}",
     "n2": "FP8 E4M3 per-channel-scaled decode GEMV, bf16 activations, (N,K) in "
           "{(17408,5120),(5120,17408),(10240,5120)} x M in {1,4,16}",
     "n4": "BF16 dense decode GEMV (unquantised weights), (N,K) in {(17408,5120),(5120,17408)} x M in {1,4,16}",
 }
 # the arithmetic type of each workload's weights
-DTYPES = {"c0": "int8", "c1": "int8", "c2": "fp8", "c3": "fp4", "c4": "fp8/fp4", "n2": "fp8", "n3": "fp4", "n4": "bf16"}
+DTYPES = {"c0": "int8", "c1": "int8", "c2": "fp8", "c3": "fp4", "c4": "fp8/fp4", "n1": "int8", "n2": "fp8", "n3": "fp4", "n4": "bf16"}
 
 
 # ----------------------------------------------------------------------------- bytes / flops
@@ -348,6 +350,18 @@ def build_n4(ql, torch):
     return Workload("n4", calls, len(calls), cfg)
 
 
+N1_MS = [32, 64, 128, 256]
+
+
+def build_n1(ql, torch):
+    """INT8 W8A8 for M > 16 (a NEXT row): the tcgen05 GEMM, two launches per call."""
+    w = build_c1(ql, torch, shapes=C1_SHAPES, Ms=N1_MS, name="n1")
+    w.launches_per_step = 2 * len(w.calls)  # quantisation + GEMM
+    for c in w.calls:
+        c["kind"] = "int8_tcgen05"
+    return w
+
+
 N2_SHAPES = C1_SHAPES
 N2_MS = [1, 4, 16]
 
@@ -380,7 +394,7 @@ def build_n2(ql, torch):
     return Workload("n2", calls, len(calls), cfg)
 
 
-BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4": build_c4, "n2": build_n2,
+BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4": build_c4, "n1": build_n1, "n2": build_n2,
             "n3": build_n3,
             "n4": build_n4}
 
@@ -391,7 +405,8 @@ _MOE = ("MoE launches per call (gate_up with the routing fused in, down, combine
         "experts / event time per call")
 KERNEL_DESC = {"c0": _SKINNY, "c1": _SKINNY, "c2": _SKINNY, "n2": _SKINNY, "n4": _SKINNY,
                "c3": _MOE, "n3": _MOE,
-               "c4": "tcgen05 block-scaled GEMM + its activation-quantisation launch; bytes / event time per call"}
+               "c4": "tcgen05 block-scaled GEMM + its activation-quantisation launch; bytes / event time per call",
+               "n1": "INT8 tcgen05 GEMM + its per-token quantisation launch; bytes / event time per call"}
 
 
 # ----------------------------------------------------------------------------- timing
@@ -490,10 +505,10 @@ def oracle_sample(config, rows_per_call):
     from oracle import qlinear_oracle as Q
     sec = 0.0
     done = 0.0
-    if config in ("c0", "c1"):
-        shapes, Ms = ([(512, 1024)], [1]) if config == "c0" else (C1_SHAPES, C1_MS)
+    if config in ("c0", "c1", "n1"):
+        shapes, Ms = {"c0": ([(512, 1024)], [1]), "c1": (C1_SHAPES, C1_MS), "n1": (C1_SHAPES, N1_MS)}[config]
         for (N, K) in shapes:
-            c = _case(("int8", N, K), lambda: synth.int8_case(16, N, K, seed=0))
+            c = _case(("int8", N, K, max(Ms)), lambda: synth.int8_case(max(Ms), N, K, seed=0))
             rows = np.arange(min(rows_per_call, N))
             for M in Ms:
                 t = time.perf_counter()
@@ -640,7 +655,7 @@ def main():
 
     import torch
     if args.steps is None:
-        args.steps = {"c0": 20000, "c1": 4000, "c2": 4000, "c3": 2000, "c4": 2000, "n2": 3000, "n3": 2000,
+        args.steps = {"c0": 20000, "c1": 4000, "c2": 4000, "c3": 2000, "c4": 2000, "n1": 2000, "n2": 3000, "n3": 2000,
                       "n4": 2000}[args.config]
     torch.cuda.set_device(local)
     pg = None
@@ -693,7 +708,7 @@ def main():
                 "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)",
                 "kernel": KERNEL_DESC[args.config],
                 "algorithmic_bytes_per_step": tot_b}
-    if args.config == "c4":
+    if args.config in ("c4", "n1"):
         fl = sum(c["flops"] for c in wl.calls)
         roofline["tensor_tflops"] = round(fl / (tot_us * 1e-6) / 1e12, 1)
 
