@@ -387,3 +387,70 @@ def moe_mxfp4(x_bits, logits_bits, w13, s13, w2, s2, I, topk, renormalize=False,
     st1 = moe_gate_up(x_bits, ids, w13, s13, I, alpha=alpha, limit=limit)
     y, y64, a = moe_down_combine(st1["h"], ids, w, w2, s2)
     return {"ids": ids, "weights": w, "stage1": st1, "y": y, "y_f64": y64, "abs_sum": a}
+
+
+# ----------------------------------------------------------------------------------------
+# Grouped MoE for larger batches with 1x128 E4M3 activations ([DSV4] §0.3, the grouped batch
+# MoE path, with the activation format of the block-scaled GEMM): routing as above; each routed
+# token's x quantised per 128-K group to E4M3 with a UE8M0 scale; gate/up sums on those
+# activations; h = bf16(swiglu(g, u)); h itself quantised per 128-K group; down on that; the
+# weighted combine.
+# ----------------------------------------------------------------------------------------
+
+
+def moe_mxfp4_act_quant(x_bits, logits_bits, w13, s13, w2, s2, I, topk, renormalize=False, alpha=1.0,
+                        limit=None, ids=None, weights=None):
+    """Whole layer with quantised activations at both GEMMs.  Returns routing, the stage-1
+    values (g, u fp64 and their error scales G, U, h bits and fp64), and the stage-2 results
+    (y bits, y fp64, abs_sum) computed from the oracle's own h."""
+    if ids is None:
+        ids, weights = route_topk(logits_bits, topk, renormalize)
+    st1 = moe_gate_up_act_quant(x_bits, ids, w13, s13, I, alpha=alpha, limit=limit)
+    yb, y64, a = moe_down_combine_act_quant(st1["h"], ids, weights, w2, s2)
+    return {"ids": ids, "weights": weights, "stage1": st1, "y": yb, "y_f64": y64, "abs_sum": a}
+
+
+def moe_gate_up_act_quant(x_bits, ids, w13, s13, I, pairs=None, cols=None, alpha=1.0, limit=None):
+    """Stage 1 on 1x128-quantised activations: a = e4m3(q) * 2^(s-127) per token, then for each
+    (token m, slot j) pair g = W13[e][:I] a_m, u = W13[e][I:] a_m and h = bf16(swiglu(g, u))."""
+    q, s = quant_e4m3_1x128(x_bits)
+    H = q.shape[1]
+    a = e4m3_decode(q) * np.repeat(ue8m0_decode(s), 128, axis=1)[:, :H]
+    M, topk = ids.shape
+    pairs = np.arange(M * topk) if pairs is None else np.asarray(pairs)
+    cols = np.arange(I) if cols is None else np.asarray(cols)
+    rows = np.concatenate([cols, I + cols])
+    out = {k: np.zeros((pairs.size, cols.size)) for k in ("g", "u", "G", "U")}
+    for pi, p in enumerate(pairs):
+        m, j = divmod(int(p), topk)
+        W = mxfp4_dequant(np.asarray(w13[int(ids[m, j])])[rows], np.asarray(s13[int(ids[m, j])])[rows])
+        gu, au = W @ a[m], np.abs(W) @ np.abs(a[m])
+        n = cols.size
+        out["g"][pi], out["u"][pi] = gu[:n], gu[n:]
+        out["G"][pi], out["U"][pi] = au[:n], au[n:]
+    out["h_f64"] = swiglu(out["g"], out["u"], alpha, limit)
+    out["h"] = round_to_bf16(out["h_f64"])
+    out["q"], out["s"] = q, s
+    return out
+
+
+def moe_down_combine_act_quant(h_bits, ids, weights, w2, s2, rows=None):
+    """Stage 2 on 1x128-quantised h: o_p = W2[e_p] a2_p with a2 = e4m3(q) * 2^(s-127) of each
+    pair's h row, y[m] = bf16(sum_j weights[m,j] o_(m,j)).  Returns (y bits, y fp64, abs_sum)."""
+    q, s = quant_e4m3_1x128(h_bits)
+    I = q.shape[1]
+    a2 = e4m3_decode(q) * np.repeat(ue8m0_decode(s), 128, axis=1)[:, :I]
+    M, topk = ids.shape
+    H = np.asarray(w2[0]).shape[0]
+    rows = np.arange(H) if rows is None else np.asarray(rows)
+    weights = np.asarray(weights, dtype=np.float64)
+    y = np.zeros((M, rows.size))
+    ab = np.zeros((M, rows.size))
+    for m in range(M):
+        for j in range(topk):
+            e = int(ids[m, j])
+            W = mxfp4_dequant(np.asarray(w2[e])[rows], np.asarray(s2[e])[rows])
+            hp = a2[m * topk + j]
+            y[m] += weights[m, j] * (W @ hp)
+            ab[m] += abs(weights[m, j]) * (np.abs(W) @ np.abs(hp))
+    return round_to_bf16(y), y, ab

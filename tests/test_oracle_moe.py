@@ -204,3 +204,41 @@ def test_moe_gate_up_passes_the_clamp_through():
     assert np.all(a["g"] == 12.0) and np.all(b["g"] == 10.0)
     assert np.array_equal(a["h"], b["h"])
     assert not np.array_equal(Q.moe_gate_up(x, ids, big, s_big, I)["h"], b["h"])
+
+
+# ------------------------------------------------------------------ grouped MoE, 1x128 E4M3 activations
+def test_moe_act_quant_single_expert_is_the_dense_act_quant_linear():
+    """E = 1, top-1: stage 1 is the dense MXFP4 linear with 1x128 E4M3 activations on W13 and
+    stage 2 the same on W2 with h as the activations (a different oracle path, pinned itself)."""
+    c = synth.moe_case(5, E=1, H=256, I=128, seed=41)
+    r = Q.moe_mxfp4_act_quant(c["x"], c["logits"], c["w13"], c["s13"], c["w2"], c["s2"], I=128, topk=1)
+    d1 = Q.mxfp4_act_quant(c["x"], c["w13"][0], c["s13"][0])
+    assert np.array_equal(r["stage1"]["g"], d1["y_f64"][:, :128])
+    assert np.array_equal(r["stage1"]["u"], d1["y_f64"][:, 128:])
+    d2 = Q.mxfp4_act_quant(r["stage1"]["h"], c["w2"][0], c["s2"][0])
+    assert np.array_equal(r["y_f64"], d2["y_f64"])
+
+
+def test_moe_act_quant_lossless_x_matches_bf16_stage1():
+    """x whose every 128-group is E4M3 codes times one power of two quantises losslessly, so
+    stage 1 equals the bf16-activation MoE's stage 1."""
+    E, H, I, M, topk = 6, 256, 128, 3, 2
+    c = synth.moe_case(M, E=E, H=H, I=I, seed=42)
+    rng = np.random.default_rng(42)
+    vals = F.e4m3_decode(rng.integers(0, 0x7F, size=(M, H)).astype(np.uint8))  # finite, >= 0
+    vals = vals * np.where(rng.random((M, H)) < 0.5, -1.0, 1.0)
+    vals[:, ::128] = 448.0  # group amax 448: the UE8M0 scale is 2^0
+    x = synth.f32_to_bf16_bits((vals * 2.0 ** -4).astype(np.float32))  # exact in bf16
+    ids, _ = Q.route_topk(c["logits"], topk)
+    a = Q.moe_gate_up_act_quant(x, ids, c["w13"], c["s13"], I)
+    b = Q.moe_gate_up(x, ids, c["w13"], c["s13"], I)
+    assert np.array_equal(a["g"], b["g"]) and np.array_equal(a["u"], b["u"])
+    assert np.array_equal(a["h"], b["h"])
+
+
+def test_moe_act_quant_clamp_passes_through():
+    c = synth.moe_case(4, E=4, H=256, I=128, seed=43)
+    ids, _ = Q.route_topk(c["logits"], 2)
+    a = Q.moe_gate_up_act_quant(c["x"], ids, c["w13"], c["s13"], 128, limit=10.0)
+    assert np.array_equal(a["h_f64"], Q.swiglu(a["g"], a["u"], 1.0, 10.0))
+    assert np.any(a["g"] > 10.0)
