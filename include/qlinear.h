@@ -83,7 +83,8 @@ enum {
   QL_PATH_MOE_MXFP4 = 6,       /* routing + dispatch + gate_up/SiLU + down + combine         */
   QL_PATH_BF16_SKINNY = 7,     /* BF16 skinny GEMM (unquantised weights)                    */
   QL_PATH_FP8_CHANNEL_SKINNY = 8, /* FP8 skinny GEMM, per-channel / per-tensor fp32 scale    */
-  QL_PATH_INT8_TCGEN05 = 9       /* per-token INT8 quant + tcgen05 GEMM on exact f16 images  */
+  QL_PATH_INT8_TCGEN05 = 9,      /* per-token INT8 quant + tcgen05 GEMM on exact f16 images  */
+  QL_PATH_MOE_MXFP4_TCGEN05 = 10 /* M > 16: routing + grouped tcgen05 GEMMs, 1x128 E4M3 act  */
 };
 
 /* device status flags (bitmask) */
@@ -242,7 +243,12 @@ QL_API ql_status qlinear_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t l
  * Debug outputs (nullable): topk_ids_out int32 [M, topk], topk_w_out fp32 [M, topk],
  * h_out bf16 [M*topk, I] (row m*topk + j).
  * swiglu_alpha must be finite; swiglu_limit >= 0 (+infinity allowed), else QL_ERR_INVALID_ARG.
- * Requires 1 <= M <= 16, 1 <= topk <= min(E, 16), E <= 1024, H % 128 == 0, I % 128 == 0,
+ * Paths: M <= 16: the persistent skinny kernel with bf16 activations (routing fused into the
+ *        gate_up launch), QL_PATH_MOE_MXFP4;
+ *        M > 16: grouped tcgen05 GEMMs over the routed experts ([DSV4] §0.3 grouped batch MoE),
+ *        QL_PATH_MOE_MXFP4_TCGEN05: x and h are quantised per token and 128-K group to E4M3 with
+ *        a UE8M0 scale before their GEMMs (the activation format of qlinear_mxfp4's act_mode 1).
+ * Requires 1 <= M <= 65535, 1 <= topk <= min(E, 16), E <= 1024, H % 128 == 0, I % 128 == 0,
  * 16-byte aligned weight pointers.
  */
 QL_API ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H,

@@ -67,7 +67,7 @@ FP8_E4M3, FP8_E5M2 = 0, 1
 ACT_BF16, ACT_E4M3_1X128 = 0, 1
 PATHS = {0: "none", 1: "int8_skinny", 2: "fp8_skinny", 3: "fp8_tcgen05", 4: "mxfp4_skinny",
          5: "mxfp4_tcgen05", 6: "moe_mxfp4", 7: "bf16_skinny", 8: "fp8_channel_skinny",
-         9: "int8_tcgen05"}
+         9: "int8_tcgen05", 10: "moe_mxfp4_tcgen05"}
 
 
 class QLError(RuntimeError):

@@ -197,6 +197,39 @@ MoeLayout moe_layout(int64_t M, int64_t H, int64_t I, int E, int topk) {
   return l;
 }
 
+// grouped MoE for M > 16 on the tcgen05 path: routing, dispatch rows and tile list, the E4M3
+// activations of both expert GEMMs by dispatch row, and the fp32 gate/up and down rows by pair
+struct Moe3Layout {
+  int tt, tiles_max;
+  size_t ids, wts, counts, offsets, tiles, ntiles, pairs, pos, q_gu, s_gu, gu, q_dn, s_dn, o, total;
+};
+Moe3Layout moe3_layout(int64_t M, int64_t H, int64_t I, int E, int topk) {
+  Moe3Layout l;
+  const int64_t P = M * topk;
+  const int64_t used = P < E ? P : E;  // experts that can be routed to
+  const int64_t avg = (P + used - 1) / used;
+  int tt = (int)((avg + 15) / 16 * 16);
+  l.tt = tt < 16 ? 16 : (tt > 128 ? 128 : tt);
+  l.tiles_max = (int)((P + l.tt - 1) / l.tt + used);
+  Carver c;
+  l.ids = c.take((size_t)P * 4);
+  l.wts = c.take((size_t)P * 4);
+  l.counts = c.take((size_t)E * 4);
+  l.offsets = c.take((size_t)(E + 1) * 4);
+  l.tiles = c.take((size_t)l.tiles_max * 16);
+  l.ntiles = c.take(4);
+  l.pairs = c.take((size_t)P * 4);
+  l.pos = c.take((size_t)P * 4);
+  l.q_gu = c.take((size_t)P * H);
+  l.s_gu = c.take((size_t)P * (H / 128));
+  l.gu = c.take((size_t)P * 2 * I * 4);
+  l.q_dn = c.take((size_t)P * I);
+  l.s_dn = c.take((size_t)P * (I / 128));
+  l.o = c.take((size_t)P * H * 4);
+  l.total = c.off;
+  return l;
+}
+
 // workspace of the INT8 tcgen05 GEMM (M > 16): f16 activation codes and per-token scales
 struct I8Layout {
   size_t img, xs, total;
@@ -312,6 +345,7 @@ size_t ql_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int to
       return dense2_layout(FMT_F8E4C, Mc, N, K, 128).total;  // E4M3 and E5M2 lay out alike
     case QL_OP_MOE_MXFP4: {
       if (E <= 0 || topk <= 0) return 0;
+      if (M > 16) return moe3_layout(M, N, K, E, topk).total;
       const size_t a = moe_layout(M, N, K, E, topk).total, b = moe2_layout(M, N, K, E, topk).total;
       return a > b ? a : b;
     }
@@ -652,7 +686,7 @@ ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint1
   if ((router_logits == nullptr) == (topk_ids_in == nullptr)) return QL_ERR_INVALID_ARG;
   if (topk_ids_in && !topk_w_in) return QL_ERR_INVALID_ARG;
   if (M < 1 || H < 1 || I < 1 || E < 1 || topk < 1) return QL_ERR_INVALID_ARG;
-  if (M > 16 || topk > 16 || topk > E || E > 1024) return QL_ERR_UNSUPPORTED;
+  if (M > 65535 || topk > 16 || topk > E || E > 1024) return QL_ERR_UNSUPPORTED;
   if (H % 128 != 0 || I % 128 != 0 || H > (1 << 20) || I > (1 << 20)) return QL_ERR_UNSUPPORTED;
   if (!al16(x) || !al16(w13) || !al16(w2) || (reinterpret_cast<uintptr_t>(s13) & 3) ||
       (reinterpret_cast<uintptr_t>(s2) & 3))
@@ -660,6 +694,91 @@ ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint1
   if (!workspace || workspace_bytes < ql_workspace_bytes(QL_OP_MOE_MXFP4, M, H, I, E, topk)) return QL_ERR_WORKSPACE;
   if (!al16(workspace)) return QL_ERR_ALIGNMENT;
   cudaStream_t st = (cudaStream_t)stream;
+  if (M > 16) {
+    // larger batches: grouped tcgen05 GEMMs over the routed experts, 1x128 E4M3 activations
+    const Moe3Layout l = moe3_layout(M, H, I, E, topk);
+    MoeGroupArgs a = {};
+    a.logits = router_logits;
+    a.ids_in = topk_ids_in;
+    a.w_in = topk_w_in;
+    a.M = (int)M;
+    a.E = E;
+    a.topk = topk;
+    a.renorm = renormalize;
+    a.ids = at<int32_t>(workspace, l.ids);
+    a.wts = at<float>(workspace, l.wts);
+    a.counts = at<int32_t>(workspace, l.counts);
+    a.ids_dbg = topk_ids_out;
+    a.w_dbg = topk_w_out;
+    a.status = at<uint32_t>(workspace, 0);
+    a.tt = l.tt;
+    a.offsets = at<int32_t>(workspace, l.offsets);
+    a.tiles = at<int4>(workspace, l.tiles);
+    a.ntiles = at<int32_t>(workspace, l.ntiles);
+    a.pairs = at<int32_t>(workspace, l.pairs);
+    a.pos_of_pair = at<int32_t>(workspace, l.pos);
+    a.x = x;
+    a.ldx = H;
+    a.H = (int)H;
+    a.I = (int)I;
+    a.q_gu = at<uint8_t>(workspace, l.q_gu);
+    a.s_gu = at<uint8_t>(workspace, l.s_gu);
+    a.gu = at<float>(workspace, l.gu);
+    a.q_dn = at<uint8_t>(workspace, l.q_dn);
+    a.s_dn = at<uint8_t>(workspace, l.s_dn);
+    a.h_dbg = h_out;
+    a.act_alpha = swiglu_alpha;
+    a.act_limit = swiglu_limit;
+    cudaError_t e = launch_moe_grouped_prologue(a, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    const int P = (int)(M * topk);
+    tc::GemmArgs g = {};
+    g.grouped = 1;
+    g.fp4 = 1;
+    g.experts = E;
+    g.tiles = a.tiles;
+    g.ntiles = a.ntiles;
+    g.tiles_max = l.tiles_max;
+    g.tt = l.tt;
+    g.pairs = a.pairs;
+    g.status = a.status;
+    g.wait_limit = g_wait_limit;
+    // gate_up: rows [0, 2I) of W13[e] against the dispatch rows' x codes, fp32 rows per pair
+    g.M = P;
+    g.N = (int)(2 * I);
+    g.K = (int)H;
+    g.w = w13;
+    g.ldw = H / 2;
+    g.w_estride = 2 * I * (H / 2);
+    g.ws = s13;
+    g.lds = H / 32;
+    g.s_estride = 2 * I * (H / 32);
+    g.aq = a.q_gu;
+    g.as = a.s_gu;
+    g.out = a.gu;
+    g.ld_out = 2 * I;
+    e = tc::launch_gemm(g, st);
+    if (e == cudaSuccess) e = launch_moe_h_quant(a, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    // down: rows [0, H) of W2[e] against the dispatch rows' h codes, fp32 rows per pair
+    g.N = (int)H;
+    g.K = (int)I;
+    g.w = w2;
+    g.ldw = I / 2;
+    g.w_estride = H * (I / 2);
+    g.ws = s2;
+    g.lds = I / 32;
+    g.s_estride = H * (I / 32);
+    g.aq = a.q_dn;
+    g.as = a.s_dn;
+    g.out = at<float>(workspace, l.o);
+    g.ld_out = H;
+    e = tc::launch_gemm(g, st);
+    if (e == cudaSuccess) e = launch_moe_combine(g.out, a.ids, a.wts, (int)M, topk, (int)H, y, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (path_out) *path_out = QL_PATH_MOE_MXFP4_TCGEN05;
+    return QL_OK;
+  }
   if (moe2_ok(H, I, s13, s2)) {
     const Moe2Layout l = moe2_layout(M, H, I, E, topk);
     if ((int64_t)l.slots * (l.gu.nb > l.dn.nb ? l.gu.nb : l.dn.nb) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;

@@ -53,6 +53,14 @@ struct TcParams {
   int sf_layout;  // 0: row r at (lane r % 32 of every quadrant, column r / 32); 1: (lane r, column 0)
   int staged;     // 1: every scale byte of the CTA is copied to shared memory once, at the start
   uint32_t sc_w_bytes;  // shared-memory bytes of the staged weight scales (16-byte multiple)
+  // grouped (MoE) launches: blockIdx.y indexes a tile list built on the device
+  int grouped;
+  const int4* tiles;     // (expert, first dispatch row, rows, 0)
+  const int* ntiles;
+  const int32_t* pairs;  // dispatch row -> (token, slot) pair
+  float* out;            // fp32 [pair][ld_out]
+  int64_t ld_out;
+  int64_t s_estride;     // bytes between two experts' weight-scale arrays
 };
 
 // Staged scales, behind the mbarriers:
@@ -92,7 +100,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kBlockN;
-  const int t0 = blockIdx.y * p.tt;
+  int t0 = blockIdx.y * p.tt;
+  int expert = 0, ntok = p.M - t0;  // token columns of this tile that hold real tokens
+  if (p.grouped) {
+    // the tile list comes from the dispatch launch; a CTA beyond its end has nothing to do
+    pdl_wait();
+    if ((int)blockIdx.y >= *p.ntiles) return;
+    const int4 tl = p.tiles[blockIdx.y];
+    expert = tl.x;
+    t0 = tl.y;
+    ntok = tl.z;
+  }
+  const uint8_t* wsc = p.ws + (int64_t)expert * p.s_estride;  // this expert's weight scales
   const int nk = p.K / kBlockK;
   const uint32_t lim = p.wait_limit;
   volatile int* abort = &s_abort;
@@ -125,10 +144,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
+    // weight tile of stage kt: a 2D view, or (grouped) a 3D view with the expert outermost
+    auto load_a = [&](uint8_t* dst, int kt, uint64_t* bar) {
+      if (p.grouped)
+        tma_load_3d(dst, &tmA, kt * kBlockK, n0, expert, bar);
+      else
+        tma_load_2d(dst, &tmA, kt * kBlockK, n0, bar);
+    };
     const int pre = nk < S ? nk : S;
     for (int kt = 0; kt < pre; ++kt) {  // weights do not depend on the previous kernel
       mbar_arrive_expect_tx(&tma_full[kt], a_tx + b_bytes);
-      tma_load_2d(sA + (size_t)kt * a_bytes, &tmA, kt * kBlockK, n0, &tma_full[kt]);
+      load_a(sA + (size_t)kt * a_bytes, kt, &tma_full[kt]);
     }
     pdl_wait();  // activation codes come from the quantisation kernel
     for (int kt = 0; kt < pre; ++kt) tma_load_2d(sB + (size_t)kt * b_bytes, &tmB, kt * kBlockK, t0, &tma_full[kt]);
@@ -141,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       mbar_arrive_expect_tx(&tma_full[s], a_tx + b_bytes);
-      tma_load_2d(sA + (size_t)s * a_bytes, &tmA, kt * kBlockK, n0, &tma_full[s]);
+      load_a(sA + (size_t)s * a_bytes, kt, &tma_full[s]);
       tma_load_2d(sB + (size_t)s * b_bytes, &tmB, kt * kBlockK, t0, &tma_full[s]);
       issued = kt + 1;
     }
@@ -198,15 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = i / nk, kt = i - r * nk;  // consecutive threads: consecutive stages of a row
           const int n = n0 + r;
           const uint32_t v =
-              n < p.N ? __ldg(reinterpret_cast<const uint32_t*>(p.ws + (int64_t)n * p.lds + 4 * kt)) : 0x7F7F7F7Fu;
+              n < p.N ? __ldg(reinterpret_cast<const uint32_t*>(wsc + (int64_t)n * p.lds + 4 * kt)) : 0x7F7F7F7Fu;
           w32[kt * 128 + (r ^ (kt & 31))] = v;
         }
       } else {
-        for (int kt = tid; kt < nk; kt += nthr) sc_w[kt] = n0 < p.N ? __ldg(p.ws + (int64_t)(n0 / 128) * p.lds + kt) : 0x7F;
+        for (int kt = tid; kt < nk; kt += nthr) sc_w[kt] = n0 < p.N ? __ldg(wsc + (int64_t)(n0 / 128) * p.lds + kt) : 0x7F;
       }
       for (int i = tid; i < p.tt * nk; i += nthr) {
         const int kt = i / p.tt, t = i - kt * p.tt;  // consecutive threads: consecutive tokens
-        sc_a[i] = t0 + t < p.M ? __ldg(p.as + (int64_t)(t0 + t) * p.las + kt) : 0x7F;
+        sc_a[i] = t < ntok ? __ldg(p.as + (int64_t)(t0 + t) * p.las + kt) : 0x7F;
       }
       asm volatile("bar.sync 1, %0;" ::"r"(kThreads - 64) : "memory");
     }
@@ -244,8 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = n0 + r;
         uint32_t wv = 0x7F7F7F7Fu;
         if (n < p.N) {
-          if (p.fp4) wv = __ldg(reinterpret_cast<const uint32_t*>(p.ws + (int64_t)n * p.lds + 4 * kt));
-          else wv = rep4(__ldg(p.ws + (int64_t)(n0 / 128) * p.lds + kt));
+          if (p.fp4) wv = __ldg(reinterpret_cast<const uint32_t*>(wsc + (int64_t)n * p.lds + 4 * kt));
+          else wv = rep4(__ldg(wsc + (int64_t)(n0 / 128) * p.lds + kt));
         }
         wa[j] = wv;
       }
@@ -254,9 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int r = (p.sf_layout == 0) ? (lane + 32 * j) : (32 * q + lane);
-          const int t = t0 + sub * p.sub_n + r;
-          wb[sub][j] = (sub < p.nsub && r < p.sub_n && t < p.M) ? rep4(__ldg(p.as + (int64_t)t * p.las + kt))
-                                                                : 0x7F7F7F7Fu;
+          const int tc = sub * p.sub_n + r;  // token column
+          wb[sub][j] = (sub < p.nsub && r < p.sub_n && tc < ntok) ? rep4(__ldg(p.as + (int64_t)(t0 + tc) * p.las + kt))
+                                                                  : 0x7F7F7F7Fu;
         }
     };
 #pragma unroll
@@ -306,11 +332,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n < p.N) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int t = t0 + c0 + j;
-            if (c0 + j < p.tt && t < p.M) {
-              uint16_t yb = f32_to_bf16_rn(__uint_as_float(r[j]));
-              if (p.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + bias);
-              p.y[(int64_t)t * p.ldy + n] = yb;
+            const int tc = c0 + j;  // token column
+            if (tc < p.tt && tc < ntok) {
+              if (p.grouped) {  // fp32 row of the (token, slot) pair at this dispatch row
+                p.out[(int64_t)p.pairs[t0 + tc] * p.ld_out + n] = __uint_as_float(r[j]);
+              } else {
+                uint16_t yb = f32_to_bf16_rn(__uint_as_float(r[j]));
+                if (p.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + bias);
+                p.y[(int64_t)(t0 + tc) * p.ldy + n] = yb;
+              }
             }
           }
         }
@@ -353,6 +383,22 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, u
   return r == CUDA_SUCCESS;
 }
 
+// 3D view {inner, outer, experts} with a byte stride between experts, 128-byte swizzle
+static bool make_map3(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                      uint64_t experts, uint64_t row_bytes, uint64_t expert_bytes, uint32_t box_inner,
+                      uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, outer, experts};
+  cuuint64_t strides[2] = {row_bytes, expert_bytes};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) fprintf(stderr, "qlinear: cuTensorMapEncodeTiled failed (%d)\n", (int)r);
+  return r == CUDA_SUCCESS;
+}
+
 size_t act_q_bytes(int64_t M, int64_t K) { return (size_t)M * K; }
 size_t act_s_bytes(int64_t M, int64_t K) { return (size_t)M * (K / 128); }
 
@@ -373,6 +419,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   p.fp4 = g.fp4;
   int mpad = ((g.M + 15) / 16) * 16;
   if (mpad > 256) mpad = 256;
+  if (g.grouped) mpad = g.tt;  // tiles of the caller's width, one MMA sub-tile
   p.nsub = (mpad + 127) / 128;
   p.sub_n = (((mpad + p.nsub - 1) / p.nsub) + 15) / 16 * 16;
   p.tt = p.nsub * p.sub_n;
@@ -397,12 +444,19 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   p.status = g.status;
   p.wait_limit = g.wait_limit;
   p.sf_layout = QL_SF_LAYOUT;
+  p.grouped = g.grouped;
+  p.tiles = g.tiles;
+  p.ntiles = g.ntiles;
+  p.pairs = g.pairs;
+  p.out = g.out;
+  p.ld_out = g.ld_out;
+  p.s_estride = g.grouped ? g.s_estride : 0;
 
   CUtensorMap ta, tb;
-  const bool ok_a = g.fp4 ? make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, g.w, (uint64_t)g.K, (uint64_t)g.N,
-                                     (uint64_t)g.ldw, kBlockK, kBlockN)
-                          : make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.w, (uint64_t)g.K, (uint64_t)g.N,
-                                     (uint64_t)g.ldw, kBlockK, kBlockN);
+  const CUtensorMapDataType wt = g.fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const bool ok_a = g.grouped ? make_map3(&ta, wt, g.w, (uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.experts,
+                                          (uint64_t)g.ldw, (uint64_t)g.w_estride, kBlockK, kBlockN)
+                              : make_map(&ta, wt, g.w, (uint64_t)g.K, (uint64_t)g.N, (uint64_t)g.ldw, kBlockK, kBlockN);
   const bool ok_b = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.aq, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.K,
                              kBlockK, (uint32_t)p.tt);
   if (!ok_a || !ok_b) return cudaErrorInvalidValue;
@@ -415,7 +469,8 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
     attr_set.store(1);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((g.N + kBlockN - 1) / kBlockN), (unsigned)((g.M + p.tt - 1) / p.tt), 1);
+  const unsigned gy = g.grouped ? (unsigned)g.tiles_max : (unsigned)((g.M + p.tt - 1) / p.tt);
+  cfg.gridDim = dim3((unsigned)((g.N + kBlockN - 1) / kBlockN), gy, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

@@ -21,6 +21,18 @@ struct GemmArgs {
   const uint16_t* bias;
   uint32_t* status;
   uint32_t wait_limit;
+  // grouped (MoE) launch: one weight matrix per expert, token tiles from a device-built list
+  int grouped;
+  int experts;
+  int64_t w_estride;       // bytes between two experts' weight matrices
+  int64_t s_estride;       // bytes between two experts' weight-scale arrays
+  const int4* tiles;       // (expert, first dispatch row, rows, 0)
+  const int* ntiles;       // number of valid tiles (device)
+  int tiles_max;           // host bound on *ntiles (grid height)
+  int tt;                  // token columns per tile (16..128, a multiple of 16)
+  const int32_t* pairs;    // dispatch row -> pair
+  float* out;              // fp32 [pairs][ld_out]
+  int64_t ld_out;
 };
 
 size_t act_q_bytes(int64_t M, int64_t K);

@@ -57,6 +57,38 @@ cudaError_t launch_skinny2(int fmt, const Skinny2Plan& p, const Skinny2Args& a, 
 cudaError_t launch_moe2(int kind, const Skinny2Plan& p, const Skinny2Args& a, const uint8_t* w, int64_t ldw,
                         int64_t w_estride, int experts, cudaStream_t st);
 
+// grouped MoE for M > 16 (kernels_moe_grouped.cu): routing, dispatch and the activation launches
+struct MoeGroupArgs {
+  const uint16_t* logits;  // bf16 [M, E] or null
+  const int32_t* ids_in;   // given routing [M, topk] or null
+  const float* w_in;
+  int M, E, topk, renorm;
+  int32_t* ids;  // [M * topk], -1 for a pair that is not dispatched
+  float* wts;
+  int32_t* counts;  // [E], zeroed by the prologue
+  int32_t* ids_dbg;
+  float* w_dbg;
+  uint32_t* status;
+  int tt;            // rows per tile of the grouped GEMMs
+  int32_t* offsets;  // [E + 1]
+  int4* tiles;       // [tiles bound]
+  int32_t* ntiles;
+  int32_t* pairs;        // dispatch row -> pair
+  int32_t* pos_of_pair;  // pair -> dispatch row (-1: none)
+  const uint16_t* x;     // bf16 [M, ldx]
+  int64_t ldx;
+  int H, I;
+  uint8_t* q_gu;  // E4M3 [M * topk, H] by dispatch row
+  uint8_t* s_gu;  // UE8M0 [M * topk, H / 128]
+  float* gu;      // fp32 [M * topk, 2I] by pair
+  uint8_t* q_dn;  // E4M3 [M * topk, I] by dispatch row
+  uint8_t* s_dn;  // UE8M0 [M * topk, I / 128]
+  uint16_t* h_dbg;  // bf16 [M * topk, I] by pair, or null
+  float act_alpha, act_limit;
+};
+cudaError_t launch_moe_grouped_prologue(const MoeGroupArgs& a, cudaStream_t st);
+cudaError_t launch_moe_h_quant(const MoeGroupArgs& a, cudaStream_t st);
+
 // split-K choice of the skinny kernel (shared by the workspace query and the launch)
 struct SplitK {
   int ks, kc;

@@ -8,6 +8,7 @@
 // Both kernels trigger the dependent GEMM launch at entry (programmatic dependent launch), so
 // the GEMM starts streaming its weights while the activations are being quantised.
 #include "internal.h"
+#include "quant_e4m3.cuh"
 
 namespace ql {
 
@@ -64,13 +65,6 @@ __global__ void __launch_bounds__(256) quant_int8_kernel(const uint16_t* __restr
   }
 }
 
-// two fp32 -> two E4M3 codes (v0 in the low byte), round to nearest even, saturating
-__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float v0, float v1) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v1), "f"(v0));
-  return r;
-}
-
 // one warp per (token, 128-group); lane holds 4 consecutive values
 __global__ void __launch_bounds__(256) quant_e4m3_kernel(const uint16_t* __restrict__ x, int M, int K, int64_t ldx,
                                                          uint8_t* __restrict__ q, int64_t ldq,
@@ -86,26 +80,12 @@ __global__ void __launch_bounds__(256) quant_e4m3_kernel(const uint16_t* __restr
   const uint2 v = *reinterpret_cast<const uint2*>(x + (int64_t)m * ldx + k);
   const float f[4] = {__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
                       __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u)};
-  float amax = fmaxf(fmaxf(fabsf(f[0]), fabsf(f[1])), fmaxf(fabsf(f[2]), fabsf(f[3])));
-  amax = warp_max(amax);
-  int e = 0;
-  if (amax > 0.f) {
-    // start two below the answer and step up: smallest e with amax <= 448 * 2^e (exact tests)
-    const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
-    e = ex - 9;
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (amax > ldexpf(448.0f, e)) ++e;
-  }
-  e = max(e, -127);
-  const float inv = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, e in [-127, 126]
-  const uint32_t c01 = f32x2_to_e4m3x2(f[0] * inv, f[1] * inv);
-  const uint32_t c23 = f32x2_to_e4m3x2(f[2] * inv, f[3] * inv);
-  const uint32_t codes = (c01 & 0xFFFFu) | (c23 << 16);
+  uint32_t sb;
+  const uint32_t codes = e4m3_group_encode(f, sb);
   *reinterpret_cast<uint32_t*>(q + (int64_t)m * ldq + k) = codes;
   if (q_dbg) *reinterpret_cast<uint32_t*>(q_dbg + (int64_t)m * K + k) = codes;
   if (lane == 0) {
-    const uint8_t b = (uint8_t)(127 + e);
+    const uint8_t b = (uint8_t)sb;
     if (s_transposed) s[(int64_t)gi * lds + m] = b;
     else s[(int64_t)m * lds + gi] = b;
     if (s_dbg) s_dbg[(int64_t)m * ng + gi] = b;

@@ -63,3 +63,18 @@ def sample_rows(N, n=48, seed=0):
     g = np.random.default_rng(seed)
     r = np.unique(np.concatenate([[0, N - 1, N // 2], g.integers(0, N, n)]))
     return r
+
+
+def h_tolerance(st, alpha=1.0, limit=None):
+    """|dh| <= 1e-3 (1.1 alpha |u_c| G + |silu(alpha g_c)| U) + 1.1e-6 alpha G U + 2^-20 |h|
+    + ulp(h): the float bar on g and u (1e-3 * sum|w x|) carried through
+    h = silu(alpha g_c) * u_c, where g_c = min(g, limit) and u_c = clip(u, +-limit) are
+    1-Lipschitz in g and u and |d silu(alpha g)/dg| <= 1.1 alpha, plus fp32 evaluation of
+    the activation and the final bf16 rounding."""
+    from oracle import qlinear_oracle as Q
+    g, u, G, U = st["g"], st["u"], st["G"], st["U"]
+    if limit is not None:
+        g, u = np.minimum(g, limit), np.clip(u, -limit, limit)
+    s = Q.silu(alpha * g)
+    return 1e-3 * (1.1 * abs(alpha) * np.abs(u) * G + np.abs(s) * U) + 1.1e-6 * abs(alpha) * G * U \
+        + 2.0 ** -20 * np.abs(s * u) + F.bf16_ulp(st["h_f64"])

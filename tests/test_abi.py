@@ -91,7 +91,7 @@ def test_moe_validation(lib):
             None]
     args = list(base); args[3] = None                  # neither logits nor ids
     assert f(*args, ctypes.byref(path)) == 1
-    args = list(base); args[1] = 17                    # M > 16
+    args = list(base); args[1] = 65536                 # M > 65535
     assert f(*args, ctypes.byref(path)) == 2
     args = list(base); args[7] = 17                    # topk > E
     assert f(*args, ctypes.byref(path)) == 2

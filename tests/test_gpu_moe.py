@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import synth
-from _util import bits_of, check_float, gpu_lib, sample_rows, to_bf16_tensor
+from _util import bits_of, check_float, gpu_lib, h_tolerance, sample_rows, to_bf16_tensor
 from oracle import formats as F
 from oracle import qlinear_oracle as Q
 
@@ -36,20 +36,6 @@ def test_mxfp4_dense_bf16(ql, M, N, K):
 
 
 # ------------------------------------------------------------------ MoE
-def h_tolerance(st, alpha=1.0, limit=None):
-    """|dh| <= 1e-3 (1.1 alpha |u_c| G + |silu(alpha g_c)| U) + 1.1e-6 alpha G U + 2^-20 |h|
-    + ulp(h): the float bar on g and u (1e-3 * sum|w x|) carried through
-    h = silu(alpha g_c) * u_c, where g_c = min(g, limit) and u_c = clip(u, +-limit) are
-    1-Lipschitz in g and u and |d silu(alpha g)/dg| <= 1.1 alpha, plus fp32 evaluation of
-    the activation and the final bf16 rounding."""
-    g, u, G, U = st["g"], st["u"], st["G"], st["U"]
-    if limit is not None:
-        g, u = np.minimum(g, limit), np.clip(u, -limit, limit)
-    s = Q.silu(alpha * g)
-    return 1e-3 * (1.1 * abs(alpha) * np.abs(u) * G + np.abs(s) * U) + 1.1e-6 * abs(alpha) * G * U \
-        + 2.0 ** -20 * np.abs(s * u) + F.bf16_ulp(st["h_f64"])
-
-
 def run_moe(ql, c, wdev, topk, ids=None, wts=None, alpha=1.0, limit=None):
     x = to_bf16_tensor(c["x"])
     kw = {}
