@@ -58,12 +58,14 @@ WORKLOADS = {
           "intermediate 2048, top-8, M in 1..9",
     "n1": "INT8 W8A8 GEMM on the tcgen05 path (per-token quantisation + kind::f16 MMAs on exact f16 images), "
           "27B-class shapes (N,K) in {(17408,5120),(5120,17408),(10240,5120)} x M in {32,64,128,256}",
+    "n5": "Grouped MXFP4 MoE on the tcgen05 path with 1x128 E4M3 activations: 256 experts, hidden 4096, "
+          "intermediate 2048, top-8, M in {32,64,128,256}",
     "n2": "FP8 E4M3 per-channel-scaled decode GEMV, bf16 activations, (N,K) in "
           "{(17408,5120),(5120,17408),(10240,5120)} x M in {1,4,16}",
     "n4": "BF16 dense decode GEMV (unquantised weights), (N,K) in {(17408,5120),(5120,17408)} x M in {1,4,16}",
 }
 # the arithmetic type of each workload's weights
-DTYPES = {"c0": "int8", "c1": "int8", "c2": "fp8", "c3": "fp4", "c4": "fp8/fp4", "n1": "int8", "n2": "fp8", "n3": "fp4", "n4": "bf16"}
+DTYPES = {"c0": "int8", "c1": "int8", "c2": "fp8", "c3": "fp4", "c4": "fp8/fp4", "n1": "int8", "n2": "fp8", "n3": "fp4", "n4": "bf16", "n5": "fp4/fp8"}
 
 
 # ----------------------------------------------------------------------------- bytes / flops
@@ -250,13 +252,14 @@ def build_c2(ql, torch):
     return Workload("c2", calls, len(calls), cfg)
 
 
-def build_c3(ql, torch, limit=None, name="c3"):
+def build_c3(ql, torch, limit=None, name="c3", Ms=None):
     from oracle import qlinear_oracle as Q  # only to count the experts each routing touches
     E, H, I, topk = 256, 4096, 2048, 8
     w = synth.moe_weights_only(E, H, I, seed=0)
     dev = [torch.from_numpy(w[k]).cuda() for k in ("w13", "s13", "w2", "s2")]
     calls = []
-    for M in C3_MS:
+    grouped = Ms is not None  # batches above 16 tokens: the grouped tcgen05 path
+    for M in (Ms or C3_MS):
         sets = []
         for r in range(ROTATE):  # different routings per rotation: different experts, cold L2
             t = synth.moe_tokens(M, E, H, seed=100 + 10 * M + r)
@@ -273,10 +276,21 @@ def build_c3(ql, torch, limit=None, name="c3"):
         uniq = float(np.mean([s[2] for s in sets]))
         b = uniq * bytes_moe_expert(H, I) + 2 * M * H * 2 + 2 * M * E
         calls.append({"fn": call, "M": M, "N": H, "K": I, "bytes": b, "flops": 2 * M * topk * 3 * H * I,
-                      "x": sets[0][0], "y": y, "kind": "moe", "unique_experts": uniq})
+                      "x": sets[0][0], "y": y, "kind": "moe_tcgen05" if grouped else "moe",
+                      "unique_experts": uniq})
     cfg = {"workload": WORKLOADS[name],
            "bytes": "unique touched experts x 13369344 B + x + logits + y"}
-    return Workload(name, calls, 3 * len(calls), cfg)  # gate_up (with routing), down, combine
+    # skinny path: gate_up (with routing), down, combine; grouped path: routing, dispatch,
+    # quantise-and-scatter, gate_up GEMM, h quantisation, down GEMM, combine
+    return Workload(name, calls, (7 if grouped else 3) * len(calls), cfg)
+
+
+N5_MS = [32, 64, 128, 256]
+
+
+def build_n5(ql, torch):
+    """Grouped MoE for larger batches on the tcgen05 path (a NEXT row)."""
+    return build_c3(ql, torch, name="n5", Ms=N5_MS)
 
 
 def build_n3(ql, torch):
@@ -395,7 +409,7 @@ def build_n2(ql, torch):
 
 
 BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4": build_c4, "n1": build_n1, "n2": build_n2,
-            "n3": build_n3,
+            "n3": build_n3, "n5": build_n5,
             "n4": build_n4}
 
 _SKINNY = ("skinny2_kernel (one launch per call: activation preparation + weight-streaming GEMM); "
@@ -405,6 +419,8 @@ _MOE = ("MoE launches per call (gate_up with the routing fused in, down, combine
         "experts / event time per call")
 KERNEL_DESC = {"c0": _SKINNY, "c1": _SKINNY, "c2": _SKINNY, "n2": _SKINNY, "n4": _SKINNY,
                "c3": _MOE, "n3": _MOE,
+               "n5": "grouped MoE launches per call (routing, dispatch, activation quantisation, two grouped "
+                     "tcgen05 GEMMs, h quantisation, combine); bytes of the touched experts / event time per call",
                "c4": "tcgen05 block-scaled GEMM + its activation-quantisation launch; bytes / event time per call",
                "n1": "INT8 tcgen05 GEMM + its per-token quantisation launch; bytes / event time per call"}
 
@@ -540,6 +556,20 @@ def oracle_sample(config, rows_per_call):
             sec += time.perf_counter() - t
             done += len(np.unique(ids)) * 2 * len(cols) * (H // 2 + H // 32)
         desc = f"MoE oracle routing + gate_up on {rows_per_call} intermediate rows for M=1 and M=9"
+    elif config == "n5":
+        E, H, I = 256, 4096, 2048
+        wsub = _case(("moe8",), lambda: synth.moe_weights_only(8, H, I, seed=0))
+        for M in (32, 256):
+            tk = _case(("tok", M), lambda: synth.moe_tokens(M, E, H, seed=0))
+            cols = np.arange(min(rows_per_call, I))
+            t = time.perf_counter()
+            ids, _ = Q.route_topk(tk["logits"], 8)
+            ids = np.asarray(ids) % 8  # 8 stand-in experts carry the sampled work
+            Q.moe_gate_up_act_quant(tk["x"], ids, wsub["w13"], wsub["s13"], I, cols=cols)
+            sec += time.perf_counter() - t
+            done += len(np.unique(ids)) * 2 * len(cols) * (H // 2 + H // 32)
+        desc = (f"grouped-MoE oracle routing + quantised gate_up on {rows_per_call} intermediate rows "
+                "for M=32 and M=256")
     elif config == "n2":
         for (N, K) in N2_SHAPES:
             c = _case(("fp8c", N, K), lambda: synth.fp8_channel_case(16, N, K, seed=0))
@@ -655,7 +685,7 @@ def main():
 
     import torch
     if args.steps is None:
-        args.steps = {"c0": 20000, "c1": 4000, "c2": 4000, "c3": 2000, "c4": 2000, "n1": 2000, "n2": 3000, "n3": 2000,
+        args.steps = {"c0": 20000, "c1": 4000, "c2": 4000, "c3": 2000, "c4": 2000, "n1": 2000, "n2": 3000, "n3": 2000, "n5": 200,
                       "n4": 2000}[args.config]
     torch.cuda.set_device(local)
     pg = None
