@@ -31,7 +31,7 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _run_both(ql, c):
+def _run_both(ql, c, path_code=1):
     M, K = c["x"].shape
     N = c["w"].shape[0]
     x = to_bf16_tensor(c["x"])
@@ -44,7 +44,7 @@ def _run_both(ql, c):
                       _p(acc_new), None, None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream),
                       ctypes.byref(path))
     assert st == 0, ql.lib.ql_status_string(st)
-    assert path.value == 1
+    assert path.value == path_code
     y_old, acc_old, _, _, _ = ql.qlinear_int8_w8a8(x, w, ws, debug=True)  # workspace entry point
     torch.cuda.synchronize()
     return bits_of(y_new), acc_new.cpu().numpy(), bits_of(y_old), acc_old.cpu().numpy()
@@ -59,6 +59,16 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
         assert np.array_equal(acc_new, acc_old)
         ref = Q.int8_w8a8(c["x"], c["w"], c["w_s"])
         check_float(y_new, F.bf16_to_f64(y_old), ref["abs_sum"])
+
+
+def test_noalloc_more_than_16_tokens_takes_the_gemm_path():
+    # 40 tokens: the tcgen05 GEMM (path 9); its activation image fits the 8 MiB scratch
+    ql = gpu_lib()
+    c = synth.int8_case(40, 640, 2048, seed=43)
+    y_new, acc_new, y_old, acc_old = _run_both(ql, c, path_code=9)
+    ref = Q.int8_w8a8(c["x"], c["w"], c["w_s"])
+    assert np.array_equal(acc_new, ref["acc"]) and np.array_equal(acc_old, ref["acc"])
+    assert np.array_equal(y_new, y_old)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
