@@ -18,9 +18,12 @@ def rng(seed: int, stream: int) -> np.random.Generator:
 
 
 def f32_to_bf16_bits(v) -> np.ndarray:
-    """Round fp32 samples to bf16 bit patterns (nearest, ties to even) for finite inputs."""
-    u = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    """Round fp32 samples to bf16 bit patterns (nearest, ties to even) for finite inputs.
+    In uint32: the largest finite pattern plus 0x8000 stays below 2^32."""
+    u = np.asarray(v, dtype=np.float32).view(np.uint32)
+    r = u + np.uint32(0x7FFF)
+    r += (u >> np.uint32(16)) & np.uint32(1)
+    r >>= np.uint32(16)
     return r.astype(np.uint16)
 
 
