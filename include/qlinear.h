@@ -231,6 +231,8 @@ QL_API ql_status qlinear_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t l
  *             the lower expert id), ordered by decreasing logit; weights = p[ids]
  *             (divided by their sum if renormalize != 0).  Alternatively the caller passes
  *             topk_ids_in / topk_w_in and router_logits = NULL (exactly one of the two).
+ *             The weights are fp32 exponentials over a float-float sum: within a few fp32
+ *             ulps of the exact softmax; the ids depend on logit comparisons only.
  *   dispatch: (token, slot) pairs grouped by expert, pairs of one expert in pair order.
  *   gate_up : for pair (m,j) with expert e: g = W13[e][0:I] x_m, u = W13[e][I:2I] x_m,
  *             h = bf16( silu(alpha * min(g, limit)) * clamp(u, -limit, limit) )

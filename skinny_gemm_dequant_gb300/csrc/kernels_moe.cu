@@ -1,80 +1,37 @@
 // MoE decode helpers: softmax top-k routing with grouped dispatch, and the weighted combine.
 //
 // Routing ([DSV4] §0.1, the M=1 routing fast path "Q1", and §0.3 grouped batch MoE): per token
-// p = softmax(logits) (evaluated in fp64, so the probabilities match an fp64 reference to the
-// last fp32 bit), the topk experts with the largest logits (equal logits: lower expert id
-// first), weights p[ids] (renormalised on request).  Dispatch groups the (token, slot) pairs
-// by expert (increasing id, stable in pair order) and lists the distinct experts in increasing
-// id; the expert GEMMs work on one slot per distinct expert.
-#include <atomic>
-
+// p = softmax(logits), the topk experts with the largest logits (equal logits: lower expert id
+// first), weights p[ids] (renormalised on request), by route_token_warp.  Dispatch groups the
+// (token, slot) pairs by expert (increasing id, stable in pair order) and lists the distinct
+// experts in increasing id; the expert GEMMs work on one slot per distinct expert.
 #include "internal.h"
+#include "route.cuh"
 
 namespace ql {
 
 constexpr int kRouteThreads = 512;  // one warp per token, M <= 16
 
 __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const MoeRouteArgs r) {
-  extern __shared__ float s_lg[];  // [M][E] logits (fp32, exact bf16 values)
   __shared__ int s_ids[256];
   __shared__ int s_cnt[1025];
   const int M = r.M, E = r.E, topk = r.topk;
   const int P = M * topk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint8_t* taken = reinterpret_cast<uint8_t*>(s_lg + (size_t)M * E);  // [M][E]
 
   if (r.logits) {
-    if (warp < M) {
+    if (warp < M) {  // a warp per token
       const int m = warp;
-      float mx = -INFINITY;
-      for (int e = lane; e < E; e += 32) {
-        const float v = bf16_bits_to_f32(r.logits[(int64_t)m * E + e]);
-        s_lg[m * E + e] = v;
-        taken[m * E + e] = 0;
-        mx = fmaxf(mx, v);
-      }
-      mx = warp_max(mx);
-      // exp in fp32 (within 2 ulp), summed in fp64: the probabilities stay within a few 1e-7
-      // of the fp64 softmax; the ids depend only on the (exact) logit comparisons
-      double sum = 0.0;
-      for (int e = lane; e < E; e += 32) sum += (double)expf(s_lg[m * E + e] - mx);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      const double rsum = 1.0 / sum;  // one fp64 division per token (fp64 is slow here)
-      double wsum = 0.0;
-      double pw[16];
-      for (int j = 0; j < topk; ++j) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
-        for (int e = lane; e < E; e += 32) {
-          if (taken[m * E + e]) continue;
-          const float v = s_lg[m * E + e];
-          if (v > bv || (v == bv && e < be)) { bv = v; be = e; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-          if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-        }
-        __syncwarp();
-        if (lane == 0) taken[m * E + be] = 1;
-        __syncwarp();
-        const double p = (double)expf(bv - mx) * rsum;
-        pw[j] = p;
-        wsum += p;
-        if (lane == 0) {
-          s_ids[m * topk + j] = be;
-          r.ids[m * topk + j] = be;
-        }
-      }
-      if (lane == 0) {
-        for (int j = 0; j < topk; ++j) {
-          const float w = (float)(r.renorm ? pw[j] * (1.0 / wsum) : pw[j]);
-          r.wts[m * topk + j] = w;
-          if (r.w_dbg) r.w_dbg[m * topk + j] = w;
-          if (r.ids_dbg) r.ids_dbg[m * topk + j] = s_ids[m * topk + j];
-        }
+      int id = -1;
+      float w = 0.f;
+      route_token_warp(r.logits + (int64_t)m * E, E, topk, r.renorm != 0, id, w);
+      if (lane < topk) {
+        const int p = m * topk + lane;
+        s_ids[p] = id;
+        r.ids[p] = id;
+        r.wts[p] = w;
+        if (r.ids_dbg) r.ids_dbg[p] = id;
+        if (r.w_dbg) r.w_dbg[p] = w;
       }
     }
   } else {
@@ -141,14 +98,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const MoeRoute
 }
 
 cudaError_t launch_moe_route(const MoeRouteArgs& r, cudaStream_t st) {
-  const size_t smem = r.logits ? (size_t)r.M * r.E * 5 : 0;
-  static std::atomic<int> attr_set{0};
-  if (!attr_set.load()) {
-    cudaError_t err = raise_smem_limit(moe_route_kernel);
-    if (err != cudaSuccess) return err;
-    attr_set.store(1);
-  }
-  moe_route_kernel<<<1, kRouteThreads, smem, st>>>(r);
+  moe_route_kernel<<<1, kRouteThreads, 0, st>>>(r);
   return cudaGetLastError();
 }
 

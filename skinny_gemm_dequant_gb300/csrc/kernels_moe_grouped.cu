@@ -9,13 +9,12 @@
 // its own dot product over the same K order.
 #include "internal.h"
 #include "quant_e4m3.cuh"
+#include "route.cuh"
 
 namespace ql {
 
 // ------------------------------------------------------------------ routing
-// One warp per token, the logits in registers (E <= 1024): p = exp(l - max) / sum with fp32
-// exponentials summed in fp64 and one fp64 reciprocal per token; the topk largest logits in
-// decreasing order, equal logits to the lower expert id; weights p[ids], renormalised on request.
+// One warp per token (E <= 1024), routed by route_token_warp.
 __global__ void __launch_bounds__(256) moe_route_many_kernel(const MoeGroupArgs a) {
   const int m = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (m >= a.M) return;
@@ -23,53 +22,7 @@ __global__ void __launch_bounds__(256) moe_route_many_kernel(const MoeGroupArgs 
   int my_e = -1;
   float my_w = 0.f;
   if (a.logits) {
-    float lv[32];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int e = lane + 32 * j;
-      lv[j] = e < E ? bf16_bits_to_f32(a.logits[(int64_t)m * E + e]) : -INFINITY;
-      mx = fmaxf(mx, lv[j]);
-    }
-    mx = warp_max(mx);
-    double sum = 0.0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (lane + 32 * j < E) sum += (double)expf(lv[j] - mx);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const double rsum = 1.0 / sum;
-    uint32_t taken = 0;
-    double wsum = 0.0, my_p = 0.0;
-    for (int k = 0; k < topk; ++k) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E && !((taken >> j) & 1u) && (lv[j] > bv || (lv[j] == bv && e < be))) {
-          bv = lv[j];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      const double pr = (double)expf(bv - mx) * rsum;
-      wsum += pr;
-      if (lane == k) {
-        my_e = be;
-        my_p = pr;
-      }
-    }
-    my_w = (float)(a.renorm ? my_p * (1.0 / wsum) : my_p);
+    route_token_warp(a.logits + (int64_t)m * E, E, topk, a.renorm != 0, my_e, my_w);
   } else if (lane < topk) {
     my_e = a.ids_in[(int64_t)m * topk + lane];
     my_w = a.w_in[(int64_t)m * topk + lane];

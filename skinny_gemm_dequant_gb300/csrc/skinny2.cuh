@@ -33,6 +33,7 @@
 // INT8).
 #pragma once
 #include "common.cuh"
+#include "route.cuh"
 #include "tc_ptx.cuh"
 
 namespace ql {
@@ -359,76 +360,31 @@ __device__ inline void s2_prepare_h(const Skinny2Args& a, int q, int sl, int nsl
 }
 
 // MoE routing inside the gate_up launch (softmax top-k, [DSV4] routing and grouped dispatch):
-// per token p = softmax(logits) (fp32 exponentials within 2 ulp, summed in fp64), the topk
+// per token p = softmax(logits) (route_token_warp: fp32 exponentials, a float-float sum), the topk
 // experts with the largest logits (equal logits: lower id first) and weights p[ids]
 // (renormalised on request); or the given ids and weights.  Then the pairs are grouped by expert
 // (increasing id, stable in pair order) and the distinct experts listed in increasing id.  Every
 // CTA computes the same routing into its shared memory (ids, first dispatch position per
 // expert, distinct experts, their count); CTA 0 also writes it all out.  All threads of the CTA
 // call this (E <= 1024, M*topk <= 256).
-__device__ inline void s2_route(const Skinny2Args& a, int* s_ids, double* s_pw, int* s_cnt, int* s_uniq, int* s_slot,
-                                int* s_nu) {
+__device__ inline void s2_route(const Skinny2Args& a, int* s_ids, int* s_cnt, int* s_uniq, int* s_slot, int* s_nu) {
   const int M = a.M, E = a.E, topk = a.topk, P = M * topk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const bool out = blockIdx.x == 0;
   if (a.logits) {
-    for (int m = warp; m < M; m += nw) {  // a warp per token, the logits in registers
-      float lv[32];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int e = lane + 32 * j;
-        lv[j] = e < E ? bf16_bits_to_f32(a.logits[(int64_t)m * E + e]) : -INFINITY;
-        mx = fmaxf(mx, lv[j]);
-      }
-      mx = warp_max(mx);
-      double sum = 0.0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (lane + 32 * j < E) sum += (double)expf(lv[j] - mx);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      // one fp64 division per token (fp64 is slow on this part): p = e * (1/sum) is within one
-      // fp64 ulp of e / sum, far below the fp32 weights' precision
-      const double rsum = 1.0 / sum;
-      uint32_t taken = 0;
-      double wsum = 0.0;
-      for (int k = 0; k < topk; ++k) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int e = lane + 32 * j;
-          if (e < E && !((taken >> j) & 1u) && (lv[j] > bv || (lv[j] == bv && e < be))) {
-            bv = lv[j];
-            be = e;
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-          if (ov > bv || (ov == bv && oe < be)) {
-            bv = ov;
-            be = oe;
-          }
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        const double pr = (double)expf(bv - mx) * rsum;
-        wsum += pr;
-        if (lane == 0) {
-          s_ids[m * topk + k] = be;
-          s_pw[m * topk + k] = pr;
-        }
-      }
-      __syncwarp();
-      if (out && lane < topk) {
+    for (int m = warp; m < M; m += nw) {  // a warp per token
+      int id = -1;
+      float w = 0.f;
+      route_token_warp(a.logits + (int64_t)m * E, E, topk, a.renorm != 0, id, w);
+      if (lane < topk) {
         const int pi = m * topk + lane;
-        const float w = (float)(a.renorm ? s_pw[pi] * (1.0 / wsum) : s_pw[pi]);
-        a.ids[pi] = s_ids[pi];
-        a.wts[pi] = w;
-        if (a.ids_dbg) a.ids_dbg[pi] = s_ids[pi];
-        if (a.w_dbg) a.w_dbg[pi] = w;
+        s_ids[pi] = id;
+        if (out) {
+          a.ids[pi] = id;
+          a.wts[pi] = w;
+          if (a.ids_dbg) a.ids_dbg[pi] = id;
+          if (a.w_dbg) a.w_dbg[pi] = w;
+        }
       }
     }
   } else {
@@ -502,10 +458,10 @@ __device__ inline void s2_route(const Skinny2Args& a, int* s_ids, double* s_pw, 
     }
 }
 
-// shared memory of s2_route: weights [P] double, ids [P] int, counts [E+1] int, slot experts [E]
-// int, slot of each expert [E] int, count
+// shared memory of s2_route: ids [P] int, counts [E+1] int, slot experts [E] int, slot of each
+// expert [E] int, count
 __host__ __device__ inline size_t s2_route_bytes(int P, int E) {
-  return ((size_t)P * 8 + (size_t)P * 4 + (size_t)(3 * E + 2) * 4 + 15) & ~size_t(15);
+  return ((size_t)P * 4 + (size_t)(3 * E + 2) * 4 + 15) & ~size_t(15);
 }
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, int x, int y, int z, int w,

@@ -60,13 +60,12 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
     pdl_wait();
     if constexpr (KIND == S2_MOE_GU) {
       const int P = a.M * a.topk;
-      double* s_pw = reinterpret_cast<double*>(fp8sc);  // no FP8 scale rows for MXFP4
-      int* s_ids = reinterpret_cast<int*>(s_pw + P);
+      int* s_ids = reinterpret_cast<int*>(fp8sc);  // no FP8 scale rows for MXFP4
       int* s_cnt = s_ids + P;
       int* s_uniq = s_cnt + a.E + 1;
       int* s_slot = s_uniq + a.E;
       int* s_nu = s_slot + a.E;
-      s2_route(a, s_ids, s_pw, s_cnt, s_uniq, s_slot, s_nu);
+      s2_route(a, s_ids, s_cnt, s_uniq, s_slot, s_nu);
       nu = *s_nu;
       r_uniq = s_uniq;
       r_ids = s_ids;
