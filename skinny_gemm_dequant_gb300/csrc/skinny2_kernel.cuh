@@ -416,16 +416,15 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
             float blk[MT][4];
 #pragma unroll
             for (int m = 0; m < MT; ++m) blk[m][0] = blk[m][1] = blk[m][2] = blk[m][3] = 0.f;
+            uint32_t wa[4], wb[4];  // bytes 0..3 of rows g and g+8 as f16 pairs
+            e2m1x8_to_f16x2x4(qa, wa);
+            e2m1x8_to_f16x2x4(qb, wb);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t a0 = e2m1x2_to_f16x2(qa >> (16 * h));
-              const uint32_t a2 = e2m1x2_to_f16x2(qa >> (16 * h + 8));
-              const uint32_t a1 = e2m1x2_to_f16x2(qb >> (16 * h));
-              const uint32_t a3 = e2m1x2_to_f16x2(qb >> (16 * h + 8));
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
               for (int m = 0; m < MT; ++m)
-                mma_f16_16816(blk[m], a0, a1, a2, a3, h ? xv[m].z : xv[m].x, h ? xv[m].w : xv[m].y);
-            }
+                mma_f16_16816(blk[m], wa[2 * h], wb[2 * h], wa[2 * h + 1], wb[2 * h + 1], h ? xv[m].z : xv[m].x,
+                              h ? xv[m].w : xv[m].y);
             // the group's scale bytes of rows g (byte 0) and g+8 (byte 1), decoded together
             uint32_t two;
             asm("prmt.b32 %0, %1, %2, %3;" : "=r"(two) : "r"(pc < 4 ? sa8.x : sa8.y), "r"(pc < 4 ? sb8.x : sb8.y),
