@@ -53,18 +53,19 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
-// two E4M3 bytes (low byte -> low lane) to an exact f16x2
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
-  return r;
+// the two FP8 pairs of a word (bytes 0,1 -> lo, bytes 2,3 -> hi), exact: the word is split into
+// its 16-bit halves as registers, not by masking and shifting
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, h0;\n\tcvt.rn.f16x2.e4m3x2 %1, h1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
-
-// two E5M2 bytes (low byte -> low lane) to an exact f16x2 (E5M2 is a subset of f16)
-__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint16_t two) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(two));
-  return r;
+__device__ __forceinline__ void e5m2x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+      "cvt.rn.f16x2.e5m2x2 %0, h0;\n\tcvt.rn.f16x2.e5m2x2 %1, h1;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // the four E2M1 pairs of a word (byte i -> o[i], low nibble -> low lane), exact.  Unpacking the

@@ -366,10 +366,8 @@ __global__ void __launch_bounds__(SK_THREADS, 2) skinny_gemm_kernel(const __grid
           s8x4_to_f16x2x2(A[j], a0, a2);
           s8x4_to_f16x2x2(B[j], a1, a3);
         } else {
-          a0 = e4m3x2_to_f16x2((uint16_t)(A[j] & 0xFFFFu));
-          a2 = e4m3x2_to_f16x2((uint16_t)(A[j] >> 16));
-          a1 = e4m3x2_to_f16x2((uint16_t)(B[j] & 0xFFFFu));
-          a3 = e4m3x2_to_f16x2((uint16_t)(B[j] >> 16));
+          e4m3x4_to_f16x2x2(A[j], a0, a2);
+          e4m3x4_to_f16x2x2(B[j], a1, a3);
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m) mma_f16_16816(blk[m], a0, a1, a2, a3, xf[m][2 * j], xf[m][2 * j + 1]);

@@ -447,15 +447,11 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
             const uint32_t qa = q[pc >> 1][2 * (pc & 1)], qb = q[pc >> 1][2 * (pc & 1) + 1];
             uint32_t a0, a1, a2, a3;
             if constexpr (FMT == FMT_F8E4C) {
-              a0 = e4m3x2_to_f16x2((uint16_t)(qa & 0xFFFFu));
-              a2 = e4m3x2_to_f16x2((uint16_t)(qa >> 16));
-              a1 = e4m3x2_to_f16x2((uint16_t)(qb & 0xFFFFu));
-              a3 = e4m3x2_to_f16x2((uint16_t)(qb >> 16));
+              e4m3x4_to_f16x2x2(qa, a0, a2);
+              e4m3x4_to_f16x2x2(qb, a1, a3);
             } else {
-              a0 = e5m2x2_to_f16x2((uint16_t)(qa & 0xFFFFu));
-              a2 = e5m2x2_to_f16x2((uint16_t)(qa >> 16));
-              a1 = e5m2x2_to_f16x2((uint16_t)(qb & 0xFFFFu));
-              a3 = e5m2x2_to_f16x2((uint16_t)(qb >> 16));
+              e5m2x4_to_f16x2x2(qa, a0, a2);
+              e5m2x4_to_f16x2x2(qb, a1, a3);
             }
             const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
 #pragma unroll
@@ -490,10 +486,9 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
             for (int j = 0; j < 4; ++j) {
               const int pc = 4 * hb + j;
               const uint32_t qa = q[pc >> 1][2 * (pc & 1)], qb = q[pc >> 1][2 * (pc & 1) + 1];
-              const uint32_t a0 = e4m3x2_to_f16x2((uint16_t)(qa & 0xFFFFu));
-              const uint32_t a2 = e4m3x2_to_f16x2((uint16_t)(qa >> 16));
-              const uint32_t a1 = e4m3x2_to_f16x2((uint16_t)(qb & 0xFFFFu));
-              const uint32_t a3 = e4m3x2_to_f16x2((uint16_t)(qb >> 16));
+              uint32_t a0, a1, a2, a3;
+              e4m3x4_to_f16x2x2(qa, a0, a2);
+              e4m3x4_to_f16x2x2(qb, a1, a3);
               const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
 #pragma unroll
               for (int m = 0; m < MT; ++m) {
