@@ -172,6 +172,12 @@ __device__ __forceinline__ int s2_cta_of(int64_t s, int64_t T, int G) {
   return (int)(((s + 1) * G + T - 1) / T) - 1;
 }
 
+// MMA token column j (0..7 within each group of 8) reads activation row rho(j), the 3-bit bit
+// reversal of j.  A quarter warp (128-bit loads) or half warp (64-bit loads) then reads rows
+// whose 128B-swizzle patterns differ in the bits that separate its 16-byte chunks, so the
+// activation loads are free of bank conflicts.  The epilogue maps column j back to token rho(j).
+__host__ __device__ __forceinline__ int s2_rho(int j) { return ((j & 1) << 2) | (j & 2) | ((j >> 2) & 1); }
+
 // swizzled byte offset of (row, byte) inside a TMA tile of 128-byte rows (128B swizzle)
 __device__ __forceinline__ uint32_t sw128(int row, int byte) {
   return (uint32_t)(row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15)));

@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
     }
   }
   const int g = lane >> 2, t = lane & 3;
+  const int gx = s2_rho(g);  // the activation row this thread's MMA column reads
   const int w = warp;  // 16-row tile of the unit
   // ldmatrix addressing: lane L feeds row 16w + (L & 7) + 8*((L >> 3) & 1) of piece 2p + (L >> 4)
   const int lrow = 16 * w + (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
     for (int m = 0; m < MT; ++m)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
-        const int col = 2 * t + e2 + 8 * m;
+        const int col = s2_rho(2 * t + e2) + 8 * m;  // the token of MMA column 2t + e2
         colf[m][e2] = col < cnt ? (kBF16 ? 1.f : a.tokf[(KIND == S2_MOE_DN ? eu * a.slot_rows : 0) + col]) : 0.f;
       }
     float rowf[2] = {1.f, 1.f}, rowb[2] = {0.f, 0.f};
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
     for (int m = 0; m < MT; ++m)
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int col = 2 * t + (r & 1) + 8 * m;
+        const int col = s2_rho(2 * t + (r & 1)) + 8 * m;  // token
         const int row = row_w + g + (r >= 2 ? 8 : 0);
         if (row >= a.N || col >= cnt) continue;
         if constexpr (KIND == S2_MOE_GU) {
@@ -394,8 +395,8 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
               const uint32_t xs = xt + ck * X_BOX;
-              const uint32_t b0 = lds32(xs + sw128(g + 8 * m, 32 * p + 4 * t));
-              const uint32_t b1 = lds32(xs + sw128(g + 8 * m, 32 * p + 16 + 4 * t));
+              const uint32_t b0 = lds32(xs + sw128(gx + 8 * m, 32 * p + 4 * t));
+              const uint32_t b1 = lds32(xs + sw128(gx + 8 * m, 32 * p + 16 + 4 * t));
               mma_bf16_16816(acc[m], q[p][0], q[p][1], q[p][2], q[p][3], b0, b1);
             }
         } else if constexpr (FMT == FMT_MXFP4) {
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
             uint4 xv[MT];
 #pragma unroll
             for (int m = 0; m < MT; ++m)
-              xv[m] = lds128(xt + (4 * ck + (kx >> 6)) * X_BOX + sw128(g + 8 * m, (kx & 63) * 2));
+              xv[m] = lds128(xt + (4 * ck + (kx >> 6)) * X_BOX + sw128(gx + 8 * m, (kx & 63) * 2));
             float blk[MT][4];
 #pragma unroll
             for (int m = 0; m < MT; ++m) blk[m][0] = blk[m][1] = blk[m][2] = blk[m][3] = 0.f;
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
             const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-              const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(g + 8 * m, (kx & 63) * 2));
+              const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(gx + 8 * m, (kx & 63) * 2));
               mma_f16_16816(ui[pc & 1][m], a0, a1, a2, a3, xv.x, xv.y);
             }
           }
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
             const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-              const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(g + 8 * m, (kx & 63) * 2));
+              const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(gx + 8 * m, (kx & 63) * 2));
               mma_f16_16816(ui[pc & 1][m], a0, a1, a2, a3, xv.x, xv.y);
             }
           }
@@ -492,7 +493,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
               const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
 #pragma unroll
               for (int m = 0; m < MT; ++m) {
-                const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(g + 8 * m, (kx & 63) * 2));
+                const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(gx + 8 * m, (kx & 63) * 2));
                 mma_f16_16816(blk[j & 1][m], a0, a1, a2, a3, xv.x, xv.y);
               }
             }
