@@ -51,14 +51,36 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, c = blockIdx.x;
+  // the activation image: the consumer warps of CTAs c, c + G, ... each write one (row, slice)
+  // job and count them in with one release (the rows are read by TMA, the async proxy, in other
+  // CTAs: proxy fence first; the release is cumulative over the CTA's writes, ordered before it
+  // by the barrier)
+  __shared__ float s_red[S2_CONSUMERS];
+  auto run_jobs = [&](int njob_rows, int nsl) {
+    unsigned mine = 0;
+    for (int j = c; j < njob_rows * nsl; j += G, ++mine) {
+      if constexpr (KIND == S2_MOE_DN)
+        s2_prepare_h(a, j % njob_rows, j / njob_rows, nsl, threadIdx.x, s_red);
+      else
+        s2_prepare<FMT>(a, j % njob_rows, j / njob_rows, nsl, threadIdx.x, s_red);
+    }
+    if (mine) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      consumer_sync();
+      if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a.ready), "r"(mine) : "memory");
+    }
+  };
   // MoE: the units follow the distinct routed experts.  gate_up routes here (every CTA alike,
-  // into shared memory behind the ring); down reads what gate_up's CTA 0 wrote.
+  // into shared memory behind the ring); down reads what gate_up's CTA 0 wrote.  gate_up's
+  // activation image needs no routing: its jobs run first, before this grid's weight stream
+  // (which starts after routing) competes with their loads and stores.
   int nu = 1;
   const int32_t* r_uniq = a.uniq;  // expert of each slot
   const int32_t* r_ids = a.ids;    // expert of each pair
   if constexpr (kMoE) {
     pdl_wait();
     if constexpr (KIND == S2_MOE_GU) {
+      if (warp < S2_CONSUMERS) run_jobs(a.M, s2_slices(a.M, G));
       const int P = a.M * a.topk;
       int* s_ids = reinterpret_cast<int*>(fp8sc);  // no FP8 scale rows for MXFP4
       int* s_cnt = s_ids + P;
@@ -241,25 +263,9 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
   }
   // -------------------------------------------------------------- consumer warps
   // activations may come from the previous kernel in the stream: wait for it, then write this
-  // CTA's jobs of the activation image (jobs j = c, c + G, ... of rows x slices), count them in
+  // CTA's jobs of the activation image (gate_up wrote them before routing)
   pdl_wait();
-  {
-    __shared__ float s_red[S2_CONSUMERS];
-    unsigned mine = 0;
-    for (int j = c; j < njob_rows * nsl; j += G, ++mine) {
-      if constexpr (KIND == S2_MOE_DN)
-        s2_prepare_h(a, j % njob_rows, j / njob_rows, nsl, threadIdx.x, s_red);
-      else
-        s2_prepare<FMT>(a, j % njob_rows, j / njob_rows, nsl, threadIdx.x, s_red);
-    }
-    if (mine) {
-      // the rows are read by TMA (async proxy) in other CTAs: proxy fence, then one release
-      // (cumulative over the CTA's writes, ordered before it by the barrier)
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      consumer_sync();
-      if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(a.ready), "r"(mine) : "memory");
-    }
-  }
+  if constexpr (KIND != S2_MOE_GU) run_jobs(njob_rows, nsl);
   const int g = lane >> 2, t = lane & 3;
   const int gx = s2_rho(g);  // the activation row this thread's MMA column reads
   const int w = warp;  // 16-row tile of the unit
