@@ -38,7 +38,7 @@ cudaError_t launch_moe_combine(const float* o, const int32_t* ids, const float* 
                                uint16_t* y, cudaStream_t st);
 
 // persistent TMA-fed skinny GEMM (skinny2.cuh); its activation image is written kXCopies times
-constexpr int kXCopies = 8;
+constexpr int kXCopies = 2;
 struct Skinny2Plan {
   int mt, mp;             // token tiles of 8, padded token rows
   int64_t nb;             // 128-row blocks
