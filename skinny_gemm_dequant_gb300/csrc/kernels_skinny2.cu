@@ -24,7 +24,7 @@ Skinny2Plan skinny2_plan(int fmt, int64_t M, int64_t N, int64_t K, int block_n, 
   p.nk = (int)((K + kpu - 1) / kpu);
   p.kpad = (int64_t)p.nk * kpu;
   p.total = slots * p.nb * p.nk;
-  const int64_t sms = (int64_t)kNumSMs * s2_ctas_per_sm(p.mt);  // fixed: workspace query and launch agree
+  const int64_t sms = (int64_t)kNumSMs * s2_ctas_per_sm(fmt, p.mt);  // fixed: workspace query and launch agree
   p.grid = (int)(p.total < sms ? p.total : sms);
   p.units_per_cta = (p.total + p.grid - 1) / p.grid;
   p.fp8_scale_bytes = 0;
@@ -92,7 +92,7 @@ static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w
   const size_t extra = p.fp8_scale_bytes + (KIND == S2_MOE_GU ? s2_route_bytes(a.M * a.topk, a.E) : 0);
   const size_t fixed = 1024 + extra + 256;  // alignment slack, extra, static
   // per CTA: the SM's 228 KB less 1 KB reserved per resident CTA, capped by the opt-in limit
-  const int optin = s2_ctas_per_sm(MT) == 1 ? 227 * 1024 : (228 * 1024) / s2_ctas_per_sm(MT) - 1024;
+  const int optin = s2_ctas_per_sm(FMT, MT) == 1 ? 227 * 1024 : (228 * 1024) / s2_ctas_per_sm(FMT, MT) - 1024;
   int S = (int)((optin - fixed) / (STAGE + 16));
   if (S > 8) S = 8;
   if (S < 2) return cudaErrorInvalidValue;

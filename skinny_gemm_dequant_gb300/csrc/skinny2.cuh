@@ -114,8 +114,11 @@ struct S2Traits {
   static constexpr int SCB = (FMT == FMT_MXFP4) ? S2_ROWS * 8 * S2_CHUNKS : 0;  // scale bytes per unit
 };
 
-// resident CTAs per SM: more warps per scheduler hide the consumers' dependency chains
-__host__ __device__ constexpr int s2_ctas_per_sm(int mt) { return mt == 1 ? 2 : 1; }
+// resident CTAs per SM: more warps per scheduler hide the consumers' dependency chains.  Two,
+// except for 9..16 tokens (MT = 2) with INT8, FP8 or BF16 weights: the MXFP4 consumers are
+// compute-bound, so their MT = 2 kernels gain from a second CTA's warps (-3.5 % on the MoE
+// decode bench), while the others lose 1.6 % (INT8 decode bench) to the halved ring per CTA.
+__host__ __device__ constexpr int s2_ctas_per_sm(int fmt, int mt) { return mt == 1 || fmt == FMT_MXFP4 ? 2 : 1; }
 
 template <int FMT, int MT>
 __host__ __device__ constexpr uint32_t s2_stage_bytes() {

@@ -23,7 +23,7 @@ namespace ql {
 // tmX: 4D view of the activation image {64 f16, img_rows, copies, kpad/64}, box {64, Mp, 1, NXB}
 //      (rows past img_rows read as zeros)
 template <int FMT, int MT, int KIND>
-__global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(MT))
+__global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
     skinny2_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
                    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Skinny2Args a) {
   using Tr = S2Traits<FMT>;

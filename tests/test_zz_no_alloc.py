@@ -74,10 +74,10 @@ def test_noalloc_more_than_16_tokens_takes_the_gemm_path():
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     ql = gpu_lib()
     f = _noalloc(ql)
-    # 16 tokens of K = 65536 need far more than 8 MiB of scratch (the activation image alone is
+    # 16 tokens of K = 262144 need far more than 8 MiB of scratch (the activation image alone is
     # 16 MiB): the call is rejected before any launch, so the placeholder addresses are never
     # touched
-    M, N, K = 16, 1024, 65536
+    M, N, K = 16, 1024, 262144
     assert ql.workspace_bytes(ql.OP_INT8_W8A8, M, N, K) > 8 << 20
     st = f(ctypes.c_void_p(16), M, K, K, ctypes.c_void_p(16), N, K, ctypes.c_void_p(16), N, None,
            ctypes.c_void_p(16), N, None, None, None, None, ctypes.byref(ctypes.c_int()))
