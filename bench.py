@@ -102,10 +102,22 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def kernel_source_hash():
+# the sources that define each configuration's kernels (device code and the host code that
+# plans their launches): a committed traffic figure holds while these files are unchanged
+_SKINNY_SRC = ("skinny.cuh", "skinny2.cuh", "skinny2_kernel.cuh", "kernels_skinny2.cu", "kernels_skinny.cu",
+               "kernels_quant.cu", "kernels_moe.cu", "route.cuh", "tc_ptx.cuh", "common.cuh", "internal.h", "api.cu")
+_TC_SRC = ("gemm_tcgen05.cu", "gemm_tcgen05.h", "kernels_quant.cu", "quant_e4m3.cuh", "tc_ptx.cuh", "common.cuh",
+           "internal.h", "api.cu")
+_I8_SRC = ("gemm_i8_tcgen05.cu", "gemm_i8_tcgen05.h", "kernels_quant.cu", "tc_ptx.cuh", "common.cuh", "internal.h",
+           "api.cu")
+KERNEL_SOURCES = {"c0": _SKINNY_SRC, "c1": _SKINNY_SRC, "c2": _SKINNY_SRC, "c3": _SKINNY_SRC, "c4": _TC_SRC,
+                  "n1": _I8_SRC, "n2": _SKINNY_SRC, "n3": _SKINNY_SRC, "n4": _SKINNY_SRC,
+                  "n5": _TC_SRC + ("kernels_moe_grouped.cu", "route.cuh", "kernels_moe.cu")}
+
+
+def kernel_source_hash(config):
     h = hashlib.sha1()
-    for f in ("skinny2.cuh", "skinny2_kernel.cuh", "kernels_skinny2.cu", "skinny.cuh", "kernels_skinny.cu",
-              "kernels_quant.cu", "kernels_moe.cu", "gemm_tcgen05.cu", "tc_ptx.cuh", "common.cuh", "api.cu"):
+    for f in KERNEL_SOURCES[config]:
         h.update(open(os.path.join(ROOT, "skinny_gemm_dequant_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:12]
 
@@ -117,7 +129,7 @@ def load_traffic(config):
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(config)
-    if not d or d.get("source_hash") != kernel_source_hash():
+    if not d or d.get("source_hash") != kernel_source_hash(config):
         return None
     return d.get("dram_bytes_per_launch")
 
