@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
   if constexpr (kMoE) {
     pdl_wait();
     if constexpr (KIND == S2_MOE_GU) {
-      if (warp < S2_CONSUMERS) run_jobs(a.M, s2_slices(a.M, G));
+      if (warp < S2_CONSUMERS) run_jobs(a.M, s2_slices(a.M, G, 8));
       const int P = a.M * a.topk;
       int* s_ids = reinterpret_cast<int*>(fp8sc);  // no FP8 scale rows for MXFP4
       int* s_cnt = s_ids + P;
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
   };
   // jobs that build the activation image, and how many of them the producers wait for
   const int njob_rows = KIND == S2_MOE_DN ? a.offsets[a.E] : (kBF16 ? 0 : a.M);
-  const int nsl = s2_slices(max(njob_rows, 1), G);
+  const int nsl = s2_slices(max(njob_rows, 1), G, kMoE ? 8 : 32);
   const unsigned need = (unsigned)(njob_rows * nsl);
 
   const int rb_first = (int)(s0 / nk);  // global row block (expert slot * nb + block)
