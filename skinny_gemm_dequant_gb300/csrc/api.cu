@@ -232,13 +232,14 @@ Moe3Layout moe3_layout(int64_t M, int64_t H, int64_t I, int E, int topk) {
 
 // workspace of the INT8 tcgen05 GEMM (M > 16): f16 activation codes and per-token scales
 struct I8Layout {
-  size_t img, xs, total;
+  size_t img, xs, part, total;
 };
-I8Layout i8_layout(int64_t M, int64_t K) {
+I8Layout i8_layout(int64_t M, int64_t N, int64_t K) {
   I8Layout l;
   Carver c;
   l.img = c.take(tc::i8_image_bytes(M, K));
   l.xs = c.take((size_t)M * 4);
+  l.part = c.take(tc::i8_part_bytes(M, N, K));  // split-K partial sums (none without a split)
   l.total = c.off;
   return l;
 }
@@ -321,7 +322,7 @@ size_t ql_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int to
   switch (op) {
     case QL_OP_INT8_W8A8: {
       const size_t a = dense2_layout(FMT_INT8, Mc, N, K, 128).total;
-      const size_t b = M > 16 ? i8_layout(M, K).total : 0;
+      const size_t b = M > 16 ? i8_layout(M, N, K).total : 0;
       return a > b ? a : b;
     }
     case QL_OP_FP8_BLOCK: {
@@ -388,7 +389,7 @@ ql_status qlinear_int8_w8a8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
 
   if (M > 16) {
     // prefill-sized batches: one GEMM on the tensor cores streams the weights once
-    const I8Layout l = i8_layout(M, K);
+    const I8Layout l = i8_layout(M, N, K);
     tc::I8GemmArgs g = {};
     g.M = (int)M;
     g.N = (int)N;
@@ -407,6 +408,8 @@ ql_status qlinear_int8_w8a8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
     g.xs_dbg = xs_out;
     g.img = at<uint16_t>(workspace, l.img);
     g.xs = at<float>(workspace, l.xs);
+    g.part = at<int32_t>(workspace, l.part);
+    g.tickets = at<unsigned>(workspace, kTicketOff);
     g.status = at<uint32_t>(workspace, 0);
     g.wait_limit = g_wait_limit;
     const cudaError_t e = tc::launch_i8_gemm(g, st);

@@ -19,6 +19,10 @@
 //   warps 4..7  : widen the int8 weight tile to the 128-byte-swizzled f16 tile the MMA reads;
 //   warps 8..15 : drain each finished 512-K group to int32 (two warps per tensor-memory lane
 //                 quadrant, half of the token columns each), then the epilogue.
+// Split K: when the 128-row x token tiles alone would leave most SMs idle (fewer than half the
+// SMs), blockIdx.z splits K into ks ranges of whole 512-K groups.  Each CTA stores its int32
+// sums in its own slot of the workspace and counts in on the tile's ticket; the CTA that completes
+// the count adds the ks slots (exact integers: the order does not matter) and runs the epilogue.
 // Every mbarrier wait is bounded; a wait that runs out raises QL_DEV_TIMEOUT in the status word,
 // the other roles stop, copies and MMAs still in flight are waited for, and tensor memory is
 // freed before the CTA exits.
@@ -45,6 +49,9 @@ constexpr uint32_t kI8DrainLimit = 1u << 22;
 
 struct I8Params {
   int M, N, K, nk, tt, stages;
+  int ks;               // K splits (gridDim.z)
+  int32_t* part;        // [ks][M][N] int32 partial sums (ks > 1)
+  unsigned* tickets;    // [tiles] arrival counts (ks > 1); zero between calls
   const float* w_s;
   int w_s_len;
   const float* x_s;
@@ -130,11 +137,17 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   uint64_t* done = bars + 3 * S + 4;   // every MMA has finished (abort path)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * 128;
   const int t0 = blockIdx.y * p.tt;
-  const int nk = p.nk;
+  // this CTA's K range: groups [g0, g1) of the call's 512-K groups, stages [kt0, kt0 + nk)
+  const int groups_all = (p.nk + kI8GroupStages - 1) / kI8GroupStages;
+  const int kz = blockIdx.z;
+  const int g0 = (int)((int64_t)kz * groups_all / p.ks), g1 = (int)((int64_t)(kz + 1) * groups_all / p.ks);
+  const int kt0 = g0 * kI8GroupStages;
+  const int nk = min(g1 * kI8GroupStages, p.nk) - kt0;
   const int ngroups = (nk + kI8GroupStages - 1) / kI8GroupStages;
   const uint32_t lim = p.wait_limit;
   volatile int* abort = &s_abort;
@@ -175,11 +188,11 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       const int pre = nk < S ? nk : S;
       for (int kt = 0; kt < pre; ++kt) {  // weights do not depend on the previous kernel
         mbar_arrive_expect_tx(&tma_full[kt], kI8A8Bytes + b_bytes);
-        tma_load_2d(stage_ptr(kt), &tmA, kt * kI8BlockK, n0, &tma_full[kt]);
+        tma_load_2d(stage_ptr(kt), &tmA, (kt0 + kt) * kI8BlockK, n0, &tma_full[kt]);
       }
       pdl_wait();  // activation codes come from the quantisation kernel
       for (int kt = 0; kt < pre; ++kt)
-        tma_load_2d(stage_ptr(kt) + kI8A8Bytes + kI8A16Bytes, &tmB, kt * kI8BlockK, t0, &tma_full[kt]);
+        tma_load_2d(stage_ptr(kt) + kI8A8Bytes + kI8A16Bytes, &tmB, (kt0 + kt) * kI8BlockK, t0, &tma_full[kt]);
       int issued = pre;
       for (int kt = pre; kt < nk; ++kt) {
         const int s = kt % S;
@@ -189,8 +202,8 @@ __global__ void __launch_bounds__(kI8Threads, 1)
           break;
         }
         mbar_arrive_expect_tx(&tma_full[s], kI8A8Bytes + b_bytes);
-        tma_load_2d(stage_ptr(s), &tmA, kt * kI8BlockK, n0, &tma_full[s]);
-        tma_load_2d(stage_ptr(s) + kI8A8Bytes + kI8A16Bytes, &tmB, kt * kI8BlockK, t0, &tma_full[s]);
+        tma_load_2d(stage_ptr(s), &tmA, (kt0 + kt) * kI8BlockK, n0, &tma_full[s]);
+        tma_load_2d(stage_ptr(s) + kI8A8Bytes + kI8A16Bytes, &tmB, (kt0 + kt) * kI8BlockK, t0, &tma_full[s]);
         issued = kt + 1;
       }
       if (*abort) {
@@ -317,9 +330,46 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[g & 1]);
     }
+    const int n = n0 + 32 * q + lane;
+    if (p.ks > 1) {
+      // split K: store this CTA's sums, count in, and let the CTA completing the count add all.
+      // Every drain warp reaches both barriers, also after a timeout (its sums are then not
+      // stored; the status word already reports the failure).
+      int32_t* slot = p.part + (int64_t)kz * p.M * p.N;
+      if (ok && n < p.N) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const int t = t0 + hcol * half + c;
+          if (c < half && t < p.M) slot[(int64_t)t * p.N + n] = sum[c];
+        }
+      }
+      __threadfence();
+      asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight drain warps
+      unsigned* ticket = p.tickets + blockIdx.y * gridDim.x + blockIdx.x;
+      if (warp == 8 && lane == 0) s_last = atomicAdd(ticket, 1u) == (unsigned)(p.ks - 1);
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      const bool last = s_last != 0;
+      if (last) {
+        __threadfence();  // the other slots were fenced before their counts
+        if (ok && n < p.N) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const int t = t0 + hcol * half + c;
+            if (c < half && t < p.M) {
+              // every slot from L2, this CTA's own included (stored and fenced above)
+              const int32_t* col = p.part + (int64_t)t * p.N + n;
+              int32_t a = 0;
+              for (int z = 0; z < p.ks; ++z) a += __ldcg(col + (int64_t)z * p.M * p.N);
+              sum[c] = a;
+            }
+          }
+        }
+        if (warp == 8 && lane == 0) *ticket = 0;  // every split has counted in: ready for the next call
+      }
+      ok = ok && last;
+    }
     if (ok) {
       pdl_wait();  // x_s comes from the quantisation kernel
-      const int n = n0 + 32 * q + lane;
       if (n < p.N) {
         const float ws = p.w_s[p.w_s_len > 1 ? n : 0];
         const float bias = p.bias ? bf16_bits_to_f32(p.bias[n]) : 0.f;
@@ -375,6 +425,29 @@ int64_t i8_kpad(int64_t K) { return (K + kI8BlockK - 1) / kI8BlockK * kI8BlockK;
 
 size_t i8_image_bytes(int64_t M, int64_t K) { return (size_t)M * i8_kpad(K) * 2; }
 
+static int64_t i8_tile_tokens(int64_t M) {
+  const int64_t mpad = (M + 15) / 16 * 16;
+  return mpad < 128 ? mpad : 128;  // token columns per CTA; more tokens take more CTAs
+}
+
+// One CTA per SM at most (shared memory), so a call with fewer output tiles than half the SMs
+// leaves most of the GPU idle: split K into whole 512-K groups until the CTAs fill the SMs once
+// (at most 8 splits, at most one split per group).
+int i8_splits(int64_t M, int64_t N, int64_t K) {
+  const int64_t tiles = (N + 127) / 128 * ((M + i8_tile_tokens(M) - 1) / i8_tile_tokens(M));
+  const int64_t groups = (i8_kpad(K) / kI8BlockK + kI8GroupStages - 1) / kI8GroupStages;
+  if (2 * tiles >= kNumSMs) return 1;
+  int64_t ks = kNumSMs / tiles;
+  if (ks > 8) ks = 8;
+  if (ks > groups) ks = groups;
+  return ks < 1 ? 1 : (int)ks;
+}
+
+size_t i8_part_bytes(int64_t M, int64_t N, int64_t K) {
+  const int ks = i8_splits(M, N, K);
+  return ks > 1 ? (size_t)ks * M * N * 4 : 0;
+}
+
 cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st) {
   const int64_t kpad = i8_kpad(g.K);
   // activation codes (exact f16), per-token scales
@@ -387,8 +460,10 @@ cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st) {
   p.N = g.N;
   p.K = g.K;
   p.nk = (int)(kpad / kI8BlockK);
-  int mpad = (g.M + 15) / 16 * 16;
-  p.tt = mpad < 128 ? mpad : 128;  // token columns per CTA; more tokens take more CTAs
+  p.tt = (int)i8_tile_tokens(g.M);
+  p.ks = i8_splits(g.M, g.N, g.K);
+  p.part = g.part;
+  p.tickets = g.tickets;
   const size_t stage = (size_t)kI8A8Bytes + kI8A16Bytes + (size_t)p.tt * kI8BlockK * 2;
   const size_t budget = 227 * 1024 - 1024 - 256;
   int S = (int)(budget / stage);
@@ -421,7 +496,7 @@ cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st) {
     attr.store(1);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((g.N + 127) / 128), (unsigned)((g.M + p.tt - 1) / p.tt), 1);
+  cfg.gridDim = dim3((unsigned)((g.N + 127) / 128), (unsigned)((g.M + p.tt - 1) / p.tt), (unsigned)p.ks);
   cfg.blockDim = dim3(kI8Threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

@@ -24,12 +24,17 @@ struct I8GemmArgs {
   float* xs_dbg;     // optional fp32 [M]
   uint16_t* img;     // workspace: f16 activation codes [M, kpad], kpad = K rounded up to 64
   float* xs;         // workspace: fp32 [M]
+  int32_t* part;     // workspace: int32 [ks][M][N] split-K partial sums (ks = i8_splits > 1)
+  unsigned* tickets; // workspace: one arrival count per output tile, zero between calls
   uint32_t* status;
   uint32_t wait_limit;
 };
 
 int64_t i8_kpad(int64_t K);
 size_t i8_image_bytes(int64_t M, int64_t K);
+// K splits of a call: more than one only when its output tiles would leave most SMs idle
+int i8_splits(int64_t M, int64_t N, int64_t K);
+size_t i8_part_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st);
 
 }  // namespace tc
