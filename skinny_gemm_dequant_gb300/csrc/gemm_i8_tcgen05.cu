@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(256) quant_i8_image_kernel(const uint16_t* __r
 // ------------------------------------------------------------------ the GEMM
 // Shared memory per stage: int8 weight tile [128][64] (plain rows) | f16 weight tile [128][64]
 // (128-byte swizzle) | f16 activation tile [tt][64] (128-byte swizzle), every part 1 KB aligned.
+// kSplit: K split over blockIdx.z (p.ks > 1); the unsplit kernel keeps the whole K and no slots
+template <bool kSplit>
 __global__ void __launch_bounds__(kI8Threads, 1)
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ I8Params p) {
@@ -144,10 +146,10 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   const int t0 = blockIdx.y * p.tt;
   // this CTA's K range: groups [g0, g1) of the call's 512-K groups, stages [kt0, kt0 + nk)
   const int groups_all = (p.nk + kI8GroupStages - 1) / kI8GroupStages;
-  const int kz = blockIdx.z;
+  const int kz = kSplit ? (int)blockIdx.z : 0;
   const int g0 = (int)((int64_t)kz * groups_all / p.ks), g1 = (int)((int64_t)(kz + 1) * groups_all / p.ks);
-  const int kt0 = g0 * kI8GroupStages;
-  const int nk = min(g1 * kI8GroupStages, p.nk) - kt0;
+  const int kt0 = kSplit ? g0 * kI8GroupStages : 0;
+  const int nk = kSplit ? min(g1 * kI8GroupStages, p.nk) - kt0 : p.nk;
   const int ngroups = (nk + kI8GroupStages - 1) / kI8GroupStages;
   const uint32_t lim = p.wait_limit;
   volatile int* abort = &s_abort;
@@ -331,7 +333,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       if (lane == 0) mbar_arrive(&acc_empty[g & 1]);
     }
     const int n = n0 + 32 * q + lane;
-    if (p.ks > 1) {
+    if constexpr (kSplit) {
       // split K: store this CTA's sums, count in, and let the CTA completing the count add all.
       // Every drain warp reaches both barriers, also after a timeout (its sums are then not
       // stored; the status word already reports the failure).
@@ -491,7 +493,8 @@ cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st) {
   const size_t smem = 1024 + (size_t)S * stage + (size_t)(3 * S + 5) * 8;
   static std::atomic<int> attr{0};
   if (!attr.load()) {
-    e = raise_smem_limit(i8_gemm_kernel);
+    e = raise_smem_limit(i8_gemm_kernel<false>);
+    if (e == cudaSuccess) e = raise_smem_limit(i8_gemm_kernel<true>);
     if (e != cudaSuccess) return e;
     attr.store(1);
   }
@@ -505,7 +508,8 @@ cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, i8_gemm_kernel, ta, tb, p);
+  return p.ks > 1 ? cudaLaunchKernelEx(&cfg, i8_gemm_kernel<true>, ta, tb, p)
+                  : cudaLaunchKernelEx(&cfg, i8_gemm_kernel<false>, ta, tb, p);
 }
 
 }  // namespace tc
