@@ -270,12 +270,12 @@ QL_API ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H,
  * has reserved all GPU memory for its pool and forbids new cudaMalloc calls, and latency-
  * critical paths that must not call cudaMalloc/cudaFree because those can synchronise the
  * device.  It computes exactly what qlinear_int8_w8a8 computes (same arguments, minus the
- * workspace) and takes its scratch from an 8 MiB array in the library's own device memory,
+ * workspace) and takes its scratch from a 16 MiB array in the library's own device memory,
  * held on every GPU that loads the library until the process exits.
  *   - The first call on each device looks up that array's device address (with the device
  *     current) and caches it; make that first call before any stream capture.
  *   - Sizes whose scratch need (ql_workspace_bytes(QL_OP_INT8_W8A8, M, N, K, 0, 0)) exceeds
- *     8 MiB are rejected with QL_ERR_WORKSPACE; nothing is launched.
+ *     16 MiB are rejected with QL_ERR_WORKSPACE; nothing is launched.
  *   - All calls on a device share the array: each call clears what must start at zero on its
  *     stream, and calls that overlap on the GPU (unordered streams) race on it.
  *   - It never calls cudaMalloc, cudaFree or any allocating routine.

@@ -25,7 +25,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr size_t kScratchBytes = size_t(16) << 20;  // 16 MiB: room for the split-K partial sums of the M > 16 GEMM
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
