@@ -50,6 +50,22 @@ def test_workspace_query(lib):
     assert f(1, -1, 1, 1, 0, 0) == 0
 
 
+def test_int8_gemm_workspace_holds_split_k_partials_only_when_k_is_split(lib):
+    """M > 16 INT8 GEMM: one CTA per 128 weight rows and token tile.  When those tiles fill fewer
+    than half of the 152 SMs, K is split (up to 8 ranges, one split per 512-K group at most) and
+    the workspace holds an int32 slot [ks][M][N] per split on top of the f16 activation image."""
+    f = lib.ql_workspace_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+    op = 1  # QL_OP_INT8_W8A8
+    image = lambda M, K: M * (-(-K // 64) * 64) * 2
+    # 5120 rows, 128 tokens: 40 tiles -> 3 splits (120 CTAs)
+    assert f(op, 128, 5120, 17408, 0, 0) >= image(128, 17408) + 3 * 128 * 5120 * 4
+    # 17408 rows: 136 tiles fill the SMs -> no split (two slots alone would exceed the bound)
+    big = f(op, 128, 17408, 5120, 0, 0)
+    assert big >= image(128, 5120) and big < image(128, 5120) + 2 * 128 * 17408 * 4
+
+
 def _int8_call(lib, **kw):
     a = dict(x=16, M=1, K=64, ldx=64, w=16, N=64, ldw=64, ws=16, wsl=64, bias=None, y=16, ldy=64,
              acc=None, xq=None, xs=None, work=16, wbytes=1 << 20)
