@@ -10,12 +10,13 @@
 //
 // Activations: the per-token preparation (INT8 quantisation, or the f16 image of bf16 values)
 // is part of this kernel, so a call is one launch.  After the grid-dependency wait, the
-// consumer warps of CTAs 0..M*copies-1 each write one (token, copy) row of an f16 image in
-// global memory, zero-padded to whole units, and count it in on a release counter; every
-// producer acquires the full count (bounded wait) before its first activation load.  The
-// weight stream does not wait: producers start loading weights as soon as the CTA starts,
-// which, with programmatic dependent launch, overlaps the previous kernel's last CTAs.  The
-// image is kept in several copies (CTA c reads copy c % copies) to spread the L2 traffic.
+// consumer warps of CTAs 0..M*slices-1 each take one (token, K slice) job: read the token's row
+// (for its amax), write the slice of its f16 image row in global memory into every copy of the
+// image (zero-padded to whole units), and count the job in on a release counter; every producer
+// acquires the full count (bounded wait) before its first activation load.  The weight stream
+// does not wait: producers start loading weights as soon as the CTA starts (MoE gate_up: once
+// it has routed), which, with programmatic dependent launch, overlaps the previous kernel's last
+// CTAs.  The image is kept in two copies (CTA c reads copy c % copies) to spread the L2 traffic.
 //
 // Inside a CTA, warp 8 is the producer.  It keeps a ring of stages in flight; a stage holds one
 // unit and is filled by two TMA operations: the weights as one 3D box (128 rows x two 128-byte
