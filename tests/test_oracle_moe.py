@@ -63,6 +63,25 @@ def test_routing_full_topk_weights_sum_to_one():
     assert np.allclose(wr.sum(1), 1.0, rtol=1e-14)
 
 
+def test_routing_signed_zeros_tie():
+    # -0 and +0 compare equal: among equal logits the lower expert id comes first
+    lg = np.array([[0x8000, 0x0000, 0xBF80, 0x8000, 0x0000]], np.uint16)  # -0, +0, -1, -0, +0
+    ids, w = Q.route_topk(lg, 4)
+    assert ids[0].tolist() == [0, 1, 3, 4]
+    assert np.all(w[0] == w[0, 0])
+
+
+def test_routing_renormalised_is_softmax_over_the_chosen():
+    # p_k / sum_{chosen} p_j: the softmax taken over the chosen logits alone
+    lg = synth.bf16_normal(synth.rng(5, 0), (4, 64))
+    ids, wr = Q.route_topk(lg, 6, renormalize=True)
+    v = F.bf16_to_f64(lg)
+    for m in range(4):
+        sel = v[m, ids[m].astype(int)]
+        e = np.exp(sel - sel.max())
+        assert np.allclose(wr[m], e / e.sum(), rtol=1e-14)
+
+
 def test_dispatch_groups_pairs():
     ids = np.array([[3, 1], [1, 0], [3, 2]], np.int32)
     off, pairs = Q.dispatch(ids, 5)
