@@ -75,7 +75,7 @@ enum {
 /* dispatch markers written to *path_out */
 enum {
   QL_PATH_NONE = 0,
-  QL_PATH_INT8_SKINNY = 1,     /* per-token INT8 quant kernel + tensor-core skinny GEMM      */
+  QL_PATH_INT8_SKINNY = 1,     /* skinny tensor-core GEMM, per-token INT8 quant in the launch */
   QL_PATH_FP8_SKINNY = 2,      /* FP8 block skinny GEMM, bf16 activations                   */
   QL_PATH_FP8_TCGEN05 = 3,     /* 1x128 act quant + tcgen05 block-scaled GEMM (FP8 x FP8)   */
   QL_PATH_MXFP4_SKINNY = 4,    /* MXFP4 skinny GEMM, bf16 activations                       */
@@ -262,6 +262,66 @@ QL_API ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H,
                             int32_t* topk_ids_out, float* topk_w_out, uint16_t* h_out,
                             uint16_t* y, void* workspace, size_t workspace_bytes,
                             ql_stream_t stream, int* path_out);
+
+/*
+ * Sharded (tensor-parallel) layers.  The pages run these linears split over 2, 4 or 8 GPUs
+ * ([Z100] chapter 一 §5, communication and parallelism under TP = 2/4/8; [DSV4] §0, TP = 4/8):
+ *   - column-parallel (N split): every shard is a plain call of the entry points above on its
+ *     rows of W (FP8 block scales: shard boundaries on whole block_n rows); the concatenated
+ *     outputs are the unsharded layer's outputs, bit for bit.
+ *   - row-parallel (K split): every shard holds a K range of W and of x (FP8 block: whole
+ *     block_k ranges; MXFP4: whole 256-K units, so its scale rows stay whole bytes per shard).
+ *     INT8: each shard's ql_token_amax, an all-reduce MAX across shards, then
+ *     qlinear_int8_w8a8_partial on each shard with that amax (its codes are then exactly the
+ *     unsharded codes), an all-reduce SUM of the int32 sums (exact) and qlinear_int8_epilogue:
+ *     the result equals the unsharded call's bit for bit.  FP8 / MXFP4: each shard's fp32
+ *     partial sums (the *_partial entry points), an all-reduce SUM, then ql_finish_f32 rounds
+ *     once to bf16 and adds the bias.  The collectives are the caller's (NCCL, gloo, ...).
+ * Pointers are device pointers owned by the caller; nothing is allocated or retained.
+ */
+
+/* Per-token amax of a K shard: amax_out[m] = max_k |x[m,k]| (fp32 [M]).  K % 8 == 0,
+ * 16-byte aligned x, ldx % 8 == 0. */
+QL_API ql_status ql_token_amax(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* amax_out,
+                               ql_stream_t stream);
+
+/* A K shard of a row-parallel INT8 W8A8 layer: x_s[m] = amax[m] / 127 (amax: the tokens'
+ * amax over the whole row, fp32 [M]), codes as in qlinear_int8_w8a8, and the exact int32
+ * sums over this shard's K written to acc_out [M, N] (dense, required); no epilogue, no y.
+ * xq_out (nullable) receives the codes.  Same requirements and workspace as
+ * qlinear_int8_w8a8. */
+QL_API ql_status qlinear_int8_w8a8_partial(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                           const int8_t* w, int64_t N, int64_t ldw, const float* amax,
+                                           int32_t* acc_out, int8_t* xq_out, void* workspace,
+                                           size_t workspace_bytes, ql_stream_t stream, int* path_out);
+
+/* The INT8 epilogue on int32 sums added over the shards: y = bf16((acc * x_s) * w_s) (+ bias
+ * after the cast), x_s = amax / 127 (IEEE fp32 division), acc int32 [M, N] dense. */
+QL_API ql_status qlinear_int8_epilogue(const int32_t* acc, int64_t M, int64_t N, const float* amax,
+                                       const float* w_scale, int64_t w_scale_len, const uint16_t* bias,
+                                       uint16_t* y, int64_t ldy, ql_stream_t stream);
+
+/* A K shard of a row-parallel FP8-block layer (bf16 activations): y32[m,n] = the fp32 sum of
+ * this shard's scaled block products (no bias), [M, ldy32].  block_k a power of two >= 64,
+ * block_n % 16 == 0; otherwise as qlinear_fp8_block with act_mode QL_ACT_BF16. */
+QL_API ql_status qlinear_fp8_block_partial(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                           const uint8_t* w, int64_t N, int64_t ldw, const uint8_t* w_scale,
+                                           int block_n, int block_k, float* y32, int64_t ldy32,
+                                           void* workspace, size_t workspace_bytes, ql_stream_t stream,
+                                           int* path_out);
+
+/* A K shard of a row-parallel MXFP4 layer (bf16 activations): fp32 partial sums into y32
+ * [M, ldy32], no bias.  K % 256 == 0, lds % 8 == 0 and 8-byte aligned w_scale (else
+ * QL_ERR_UNSUPPORTED); otherwise as qlinear_mxfp4 with act_mode QL_ACT_BF16. */
+QL_API ql_status qlinear_mxfp4_partial(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                       const uint8_t* w, int64_t N, int64_t ldw_bytes, const uint8_t* w_scale,
+                                       int64_t lds, float* y32, int64_t ldy32, void* workspace,
+                                       size_t workspace_bytes, ql_stream_t stream, int* path_out);
+
+/* One bf16 rounding of fp32 sums added over the shards, then + bias (after the cast, rounded
+ * again): y[m,n] = bf16(bf16(y32[m,n]) + bias[n]). */
+QL_API ql_status ql_finish_f32(const float* y32, int64_t M, int64_t N, int64_t ld32, const uint16_t* bias,
+                               uint16_t* y, int64_t ldy, ql_stream_t stream);
 
 /*
  * INT8 W8A8 linear that allocates nothing and takes no workspace.  The pages have no

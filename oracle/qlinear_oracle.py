@@ -53,15 +53,19 @@ def _cdiv(a: int, b: int) -> int:
 # ----------------------------------------------------------------------------------------
 
 
-def quant_int8_per_token(x_bits):
+def quant_int8_per_token(x_bits, amax=None):
     """Dynamic symmetric per-token INT8 quantisation of bf16 activations.
 
     For each token m: amax = max_k |x[m,k]| (exact in fp32), x_s = amax / 127 and
     x_q = round_half_even(x / x_s) clamped to [-127, 127], both divisions IEEE fp32.
     A token whose amax is 0 gets x_s = 0 and x_q = 0.  Returns (x_q int8 [M,K], x_s fp32 [M]).
+    ``amax`` (optional, fp32 [M]) is the tokens' amax taken over a wider K than ``x_bits``
+    holds: a K slice of a row-parallel layer quantises with the whole row's scale.
     """
     xf = bf16_to_f32(x_bits)
-    amax = np.max(np.abs(xf), axis=1).astype(np.float32)
+    if amax is None:
+        amax = np.max(np.abs(xf), axis=1).astype(np.float32)
+    amax = np.asarray(amax, dtype=np.float32).reshape(-1)
     xs = (amax / np.float32(127.0)).astype(np.float32)
     safe = np.where(xs > 0, xs, np.float32(1.0)).astype(np.float32)
     quo = (xf / safe[:, None]).astype(np.float32)
@@ -92,10 +96,11 @@ def int8_epilogue(acc, x_s, w_s, bias_bits=None):
     return yb
 
 
-def int8_w8a8(x_bits, w, w_s, bias_bits=None, rows=None):
+def int8_w8a8(x_bits, w, w_s, bias_bits=None, rows=None, amax=None):
     """Whole INT8 W8A8 linear: quantise x, accumulate exactly, epilogue.
 
-    ``rows`` (optional) restricts the computation to those output columns n.
+    ``rows`` (optional) restricts the computation to those output columns n; ``amax``
+    (optional) is the per-token amax to quantise with (see quant_int8_per_token).
     Returns dict with x_q, x_s, acc [M,len(rows)], y bits, and the error scale
     sum_k |x_deq * w_deq| used by the float tolerance."""
     w = np.asarray(w, dtype=np.int8)
@@ -106,7 +111,7 @@ def int8_w8a8(x_bits, w, w_s, bias_bits=None, rows=None):
         w_s = w_s[rows] if w_s.size > 1 else w_s
         if bias_bits is not None:
             bias_bits = np.asarray(bias_bits)[rows]
-    x_q, x_s = quant_int8_per_token(x_bits)
+    x_q, x_s = quant_int8_per_token(x_bits, amax)
     acc = int8_accumulate(x_q, w)
     y = int8_epilogue(acc, x_s, w_s, bias_bits)
     abs_acc = np.abs(x_q.astype(np.int64)) @ np.abs(w.astype(np.int64)).T

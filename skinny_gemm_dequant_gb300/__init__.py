@@ -22,6 +22,8 @@ __all__ = [
     "workspace_bytes", "Workspace", "read_device_status", "set_wait_limit",
     "OP_INT8_W8A8", "OP_FP8_BLOCK", "OP_MXFP4", "OP_MOE_MXFP4", "OP_BF16", "OP_FP8_CHANNEL", "qlinear_bf16",
     "qlinear_fp8", "FP8_E4M3", "FP8_E5M2", "ACT_BF16", "ACT_E4M3_1X128", "PATHS",
+    "token_amax", "qlinear_int8_w8a8_partial", "qlinear_int8_epilogue", "qlinear_fp8_block_partial",
+    "qlinear_mxfp4_partial", "finish_f32",
 ]
 
 if not os.path.exists(_LIB_PATH):
@@ -61,6 +63,21 @@ lib.qlinear_mxfp4.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64,
 lib.moe_mxfp4_grouped.restype = _int
 lib.moe_mxfp4_grouped.argtypes = [_vp, _i64, _i64, _vp, _vp, _vp, _int, _int, _int, _vp, _vp, _vp, _vp, _i64,
                                   ctypes.c_float, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _ip]
+
+lib.ql_token_amax.restype = _int
+lib.ql_token_amax.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp]
+lib.qlinear_int8_w8a8_partial.restype = _int
+lib.qlinear_int8_w8a8_partial.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp, _ip]
+lib.qlinear_int8_epilogue.restype = _int
+lib.qlinear_int8_epilogue.argtypes = [_vp, _i64, _i64, _vp, _vp, _i64, _vp, _vp, _i64, _vp]
+lib.qlinear_fp8_block_partial.restype = _int
+lib.qlinear_fp8_block_partial.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _int, _int, _vp, _i64, _vp,
+                                          _sz, _vp, _ip]
+lib.qlinear_mxfp4_partial.restype = _int
+lib.qlinear_mxfp4_partial.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _sz, _vp,
+                                      _ip]
+lib.ql_finish_f32.restype = _int
+lib.ql_finish_f32.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _i64, _vp]
 
 OP_INT8_W8A8, OP_FP8_BLOCK, OP_MXFP4, OP_MOE_MXFP4, OP_BF16, OP_FP8_CHANNEL = 1, 2, 3, 4, 5, 6
 FP8_E4M3, FP8_E5M2 = 0, 1
@@ -114,7 +131,8 @@ _default_ws: dict = {}
 
 def _ws(device, nbytes, stream, workspace):
     if workspace is None:
-        key = (torch.device(device).index, None if stream is None else id(stream))
+        # keyed by the stream's handle: a Python object's id can be reused once it is collected
+        key = (torch.device(device).index, None if stream is None else int(stream.cuda_stream))
         workspace = _default_ws.setdefault(key, Workspace(device))
     return workspace.get(nbytes, stream)
 
@@ -279,3 +297,83 @@ def moe_mxfp4_grouped(x, w13, s13, w2, s2, *, router_logits=None, topk_ids=None,
 
 
 _u32 = ctypes.c_uint32
+
+
+# ------------------------------------------------------------------ sharded layers
+def token_amax(x, *, out=None, stream=None):
+    """Per-token max |x| of a K shard (fp32 [M]): the row-parallel INT8 layer's all-reduce MAX
+    input."""
+    _bf16(x, "x")
+    M, K = x.shape
+    amax = out if out is not None else torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(lib.ql_token_amax(_ptr(x), M, K, x.stride(0), _ptr(amax), _stream(stream)), "ql_token_amax")
+    return amax
+
+
+def qlinear_int8_w8a8_partial(x, w, amax, *, debug=False, out=None, workspace=None, stream=None):
+    """A K shard of a row-parallel INT8 layer: exact int32 sums [M, N] over this shard's K, with
+    x_s = amax / 127 (amax: the tokens' amax over the whole row).  debug=True also returns the
+    codes and the path: (acc, x_q, path)."""
+    _bf16(x, "x")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.dtype != torch.int8 or w.stride(1) != 1 or x.stride(1) != 1:
+        raise TypeError("w must be int8 with unit inner stride; x must have unit inner stride")
+    acc = out if out is not None else torch.empty(M, N, dtype=torch.int32, device=x.device)
+    xq = torch.empty(M, K, dtype=torch.int8, device=x.device) if debug else None
+    ws = _ws(x.device, workspace_bytes(OP_INT8_W8A8, M, N, K), stream, workspace)
+    path = ctypes.c_int(0)
+    _check(lib.qlinear_int8_w8a8_partial(_ptr(x), M, K, x.stride(0), _ptr(w), N, w.stride(0), _ptr(amax), _ptr(acc),
+                                         _ptr(xq), _ptr(ws), ws.numel(), _stream(stream), ctypes.byref(path)),
+           "qlinear_int8_w8a8_partial")
+    if debug:
+        return acc, xq, PATHS[path.value]
+    return acc
+
+
+def qlinear_int8_epilogue(acc, amax, w_scale, bias=None, *, out=None, stream=None):
+    """y = bf16((acc * amax/127) * w_scale) (+ bias) on int32 sums added over the shards."""
+    M, N = acc.shape
+    y = out if out is not None else torch.empty(M, N, dtype=torch.bfloat16, device=acc.device)
+    _check(lib.qlinear_int8_epilogue(_ptr(acc), M, N, _ptr(amax), _ptr(w_scale), w_scale.numel(), _ptr(bias), _ptr(y),
+                                     y.stride(0), _stream(stream)), "qlinear_int8_epilogue")
+    return y
+
+
+def qlinear_fp8_block_partial(x, w, w_scale, *, K=None, block_n=128, block_k=128, out=None, workspace=None,
+                              stream=None):
+    """A K shard of a row-parallel FP8-block layer: fp32 partial sums [M, N] (no bias)."""
+    _bf16(x, "x")
+    M, Kx = x.shape
+    K = Kx if K is None else K
+    N = w.shape[0]
+    y32 = out if out is not None else torch.empty(M, N, dtype=torch.float32, device=x.device)
+    ws = _ws(x.device, workspace_bytes(OP_FP8_BLOCK, M, N, K), stream, workspace)
+    path = ctypes.c_int(0)
+    _check(lib.qlinear_fp8_block_partial(_ptr(x), M, K, x.stride(0), _ptr(w), N, w.stride(0), _ptr(w_scale), block_n,
+                                         block_k, _ptr(y32), y32.stride(0), _ptr(ws), ws.numel(), _stream(stream),
+                                         ctypes.byref(path)), "qlinear_fp8_block_partial")
+    return y32
+
+
+def qlinear_mxfp4_partial(x, w, w_scale, *, out=None, workspace=None, stream=None):
+    """A K shard of a row-parallel MXFP4 layer: fp32 partial sums [M, N] (no bias)."""
+    _bf16(x, "x")
+    M, K = x.shape
+    N = w.shape[0]
+    y32 = out if out is not None else torch.empty(M, N, dtype=torch.float32, device=x.device)
+    ws = _ws(x.device, workspace_bytes(OP_MXFP4, M, N, K), stream, workspace)
+    path = ctypes.c_int(0)
+    _check(lib.qlinear_mxfp4_partial(_ptr(x), M, K, x.stride(0), _ptr(w), N, w.stride(0), _ptr(w_scale),
+                                     w_scale.stride(0), _ptr(y32), y32.stride(0), _ptr(ws), ws.numel(), _stream(stream),
+                                     ctypes.byref(path)), "qlinear_mxfp4_partial")
+    return y32
+
+
+def finish_f32(y32, bias=None, *, out=None, stream=None):
+    """bf16(y32) (+ bias after the cast): the one rounding of fp32 sums added over the shards."""
+    M, N = y32.shape
+    y = out if out is not None else torch.empty(M, N, dtype=torch.bfloat16, device=y32.device)
+    _check(lib.ql_finish_f32(_ptr(y32), M, N, y32.stride(0), _ptr(bias), _ptr(y), y.stride(0), _stream(stream)),
+           "ql_finish_f32")
+    return y

@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqlinear.so")
 SOURCES = ["api.cu", "kernels_quant.cu", "kernels_skinny.cu", "kernels_moe.cu", "gemm_tcgen05.cu", "noalloc.cu",
-           "kernels_skinny2.cu", "gemm_i8_tcgen05.cu", "kernels_moe_grouped.cu"]
+           "kernels_skinny2.cu", "gemm_i8_tcgen05.cu", "kernels_moe_grouped.cu", "kernels_shard.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

@@ -11,6 +11,10 @@
 
 using namespace ql;
 
+#ifndef QL_CELL_TOKENS
+#define QL_CELL_TOKENS 4
+#endif
+
 namespace {
 
 uint32_t g_wait_limit = 1u << 20;
@@ -20,11 +24,17 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) =
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Workspace layout: [0, 256) status word (offset 0) and the skinny GEMM's activation hand-off
-// counters (offsets 32 and 36); [256, 256 + 4*kMaxTickets) split-K tickets, at the same place
-// for every op and shape, so that no call's data region ever overlaps them (the kernels return
-// every counter and ticket to zero); op regions follow, carved in order.
+// counters (offsets 32 and 36);
+// [256, 256 + 4*kMaxTickets) split-K tickets, at the same place for every op and shape, so that
+// no call's data region ever overlaps them (the kernels return every counter and ticket to
+// zero); op regions follow, carved in order.
 constexpr size_t kMaxTickets = 65536;
 constexpr size_t kReadyOff = 32, kDoneOff = 36;
+// INT8 calls of up to this many tokens settle their outputs through atomic cells (skinny2.cuh,
+// s2_cell_*); larger ones through per-CTA partial sums and a waiting settler.  Measured on the
+// INT8 decode bench: cells are faster at 1..4 tokens (most at N = 5120, K = 17408, where a row
+// block is shared by about 8 CTAs), slower at 8 and 16 (their atomic traffic grows with M)
+constexpr int64_t kCellTokens = QL_CELL_TOKENS;
 constexpr size_t kTicketOff = 256;
 constexpr size_t kRegionsOff = kTicketOff + 4 * kMaxTickets;
 
@@ -81,16 +91,18 @@ DenseLayout dense_layout(int fmt, int64_t M, int64_t N, int64_t K) {
 
 struct Dense2Layout {
   Skinny2Plan p;
-  size_t x16, sc, part, total;
+  size_t cells, x16, sc, part, total;
 };
 
 Dense2Layout dense2_layout(int fmt, int64_t Mc, int64_t N, int64_t K, int block_n) {
   Dense2Layout l;
   l.p = skinny2_plan(fmt, Mc, N, K, block_n);
   Carver c;
+  const bool cells = fmt == FMT_INT8 && Mc <= kCellTokens;
+  l.cells = c.take(cells ? (size_t)N * Mc * 8 : 0);  // INT8 output cells [M][N]
   l.x16 = c.take((size_t)kXCopies * Mc * l.p.kpad * 2);
   l.sc = c.take(16 * 4);
-  l.part = c.take((size_t)l.p.grid * 16 * S2_ROWS * 4);  // one partial slot per CTA
+  l.part = c.take(cells ? 0 : (size_t)l.p.grid * 16 * S2_ROWS * 4);  // one partial slot per CTA
   l.total = c.off;
   return l;
 }
@@ -160,6 +172,9 @@ struct Dense2Call {
   int32_t* acc_out;
   int8_t* xq_out;
   float* xs_out;
+  const float* amax_in;  // INT8 K shard: the tokens' amax over the whole row
+  float* y32;            // FP8 / MXFP4 K shard: fp32 partial sums [M, ldy32] instead of y
+  int64_t ldy32;
 };
 
 ql_status run_dense2(const Dense2Call& d, void* workspace, cudaStream_t st);
@@ -258,6 +273,8 @@ bool tc_path(int act_mode) { return act_mode == QL_ACT_E4M3_1X128; }
 
 uint32_t ql::wait_limit() { return g_wait_limit; }
 
+size_t ql::workspace_zero_bytes() { return kRegionsOff; }
+
 namespace {
 ql_status run_dense2(const Dense2Call& d, void* workspace, cudaStream_t st) {
   for (int64_t m0 = 0; m0 < d.M; m0 += 16) {
@@ -282,12 +299,16 @@ ql_status run_dense2(const Dense2Call& d, void* workspace, cudaStream_t st) {
     a.block_k = d.block_k;
     a.w_scale = d.w_scale;
     a.w_scale_len = (int)d.w_scale_len;
-    a.y = d.y + m0 * d.ldy;
+    a.y = d.y ? d.y + m0 * d.ldy : nullptr;
     a.ldy = d.ldy;
     a.bias = d.bias;
     a.acc_out = d.acc_out ? d.acc_out + m0 * d.N : nullptr;
+    a.amax_in = d.amax_in ? d.amax_in + m0 : nullptr;
+    a.y32 = d.y32 ? d.y32 + m0 * d.ldy32 : nullptr;
+    a.ldy32 = d.ldy32;
     a.part = at<float>(workspace, l.part);
     a.tickets = at<unsigned>(workspace, kTicketOff);
+    a.cells = (d.fmt == FMT_INT8 && Mc <= kCellTokens) ? at<unsigned long long>(workspace, l.cells) : nullptr;
     a.status = at<uint32_t>(workspace, 0);
     a.wait_limit = g_wait_limit;
     const cudaError_t e = launch_skinny2(d.fmt, l.p, a, d.w, d.ldw, st);
@@ -370,15 +391,19 @@ ql_status ql_read_device_status(void* workspace, ql_stream_t stream, int clear, 
   return (flags & QL_DEV_TIMEOUT) ? QL_ERR_TIMEOUT : QL_OK;
 }
 
-// ------------------------------------------------------------------ INT8 W8A8
-ql_status qlinear_int8_w8a8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const int8_t* w, int64_t N,
-                            int64_t ldw, const float* w_scale, int64_t w_scale_len, const uint16_t* bias,
-                            uint16_t* y, int64_t ldy, int32_t* acc_out, int8_t* xq_out, float* xs_out,
-                            void* workspace, size_t workspace_bytes, ql_stream_t stream, int* path_out) {
+}  // extern "C"
+
+namespace {
+// the INT8 linear; amax_in (a K shard's whole-row amax) and y == null (acc_out only) serve the
+// row-parallel layer
+ql_status int8_impl(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const int8_t* w, int64_t N, int64_t ldw,
+                    const float* w_scale, int64_t w_scale_len, const uint16_t* bias, uint16_t* y, int64_t ldy,
+                    int32_t* acc_out, int8_t* xq_out, float* xs_out, const float* amax_in, void* workspace,
+                    size_t workspace_bytes, ql_stream_t stream, int* path_out) {
   if (path_out) *path_out = QL_PATH_NONE;
-  if (!x || !w || !w_scale || !y) return QL_ERR_INVALID_ARG;
-  if (M < 1 || N < 1 || K < 1 || ldx < K || ldw < K || ldy < N) return QL_ERR_INVALID_ARG;
-  if (w_scale_len != 1 && w_scale_len != N) return QL_ERR_INVALID_ARG;
+  if (!x || !w || (y && !w_scale) || (!y && !acc_out)) return QL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldx < K || ldw < K || (y && ldy < N)) return QL_ERR_INVALID_ARG;
+  if (y && w_scale_len != 1 && w_scale_len != N) return QL_ERR_INVALID_ARG;
   if (M > 65535 || N > (1 << 30) || K > 133152) return QL_ERR_UNSUPPORTED;  // |acc| < 2^31
   if (K % 16 != 0) return QL_ERR_UNSUPPORTED;
   if (cdiv(N, SK_ROWS) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
@@ -412,6 +437,7 @@ ql_status qlinear_int8_w8a8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
     g.tickets = at<unsigned>(workspace, kTicketOff);
     g.status = at<uint32_t>(workspace, 0);
     g.wait_limit = g_wait_limit;
+    g.amax_in = amax_in;
     const cudaError_t e = tc::launch_i8_gemm(g, st);
     if (e != cudaSuccess) return cuda_status(e);
     if (path_out) *path_out = QL_PATH_INT8_TCGEN05;
@@ -435,10 +461,62 @@ ql_status qlinear_int8_w8a8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
   d.acc_out = acc_out;
   d.xq_out = xq_out;
   d.xs_out = xs_out;
+  d.amax_in = amax_in;
   const ql_status s = run_dense2(d, workspace, st);
   if (s != QL_OK) return s;
   if (path_out) *path_out = QL_PATH_INT8_SKINNY;
   return QL_OK;
+}
+}  // namespace
+
+extern "C" {
+
+// ------------------------------------------------------------------ INT8 W8A8
+ql_status qlinear_int8_w8a8(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const int8_t* w, int64_t N,
+                            int64_t ldw, const float* w_scale, int64_t w_scale_len, const uint16_t* bias,
+                            uint16_t* y, int64_t ldy, int32_t* acc_out, int8_t* xq_out, float* xs_out,
+                            void* workspace, size_t workspace_bytes, ql_stream_t stream, int* path_out) {
+  if (path_out) *path_out = QL_PATH_NONE;
+  if (!y) return QL_ERR_INVALID_ARG;
+  return int8_impl(x, M, K, ldx, w, N, ldw, w_scale, w_scale_len, bias, y, ldy, acc_out, xq_out, xs_out, nullptr,
+                   workspace, workspace_bytes, stream, path_out);
+}
+
+// ------------------------------------------------------------------ sharded layers
+ql_status ql_token_amax(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, float* amax_out, ql_stream_t stream) {
+  if (!x || !amax_out) return QL_ERR_INVALID_ARG;
+  if (M < 1 || K < 1 || ldx < K) return QL_ERR_INVALID_ARG;
+  if (M > 65535 || K > (1 << 30)) return QL_ERR_UNSUPPORTED;
+  if (K % 8 != 0) return QL_ERR_UNSUPPORTED;
+  if (!al16(x) || ldx % 8 != 0) return QL_ERR_ALIGNMENT;
+  return cuda_status(launch_token_amax(x, (int)M, (int)K, ldx, amax_out, (cudaStream_t)stream));
+}
+
+ql_status qlinear_int8_w8a8_partial(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const int8_t* w,
+                                    int64_t N, int64_t ldw, const float* amax, int32_t* acc_out, int8_t* xq_out,
+                                    void* workspace, size_t workspace_bytes, ql_stream_t stream, int* path_out) {
+  if (path_out) *path_out = QL_PATH_NONE;
+  if (!amax || !acc_out) return QL_ERR_INVALID_ARG;
+  return int8_impl(x, M, K, ldx, w, N, ldw, nullptr, 0, nullptr, nullptr, 0, acc_out, xq_out, nullptr, amax,
+                   workspace, workspace_bytes, stream, path_out);
+}
+
+ql_status qlinear_int8_epilogue(const int32_t* acc, int64_t M, int64_t N, const float* amax, const float* w_scale,
+                                int64_t w_scale_len, const uint16_t* bias, uint16_t* y, int64_t ldy,
+                                ql_stream_t stream) {
+  if (!acc || !amax || !w_scale || !y) return QL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || ldy < N || (w_scale_len != 1 && w_scale_len != N)) return QL_ERR_INVALID_ARG;
+  if (M > 65535 || N > (1 << 30)) return QL_ERR_UNSUPPORTED;
+  return cuda_status(launch_int8_epilogue(acc, (int)M, (int)N, amax, w_scale, (int)w_scale_len, bias, y, ldy,
+                                          (cudaStream_t)stream));
+}
+
+ql_status ql_finish_f32(const float* y32, int64_t M, int64_t N, int64_t ld32, const uint16_t* bias, uint16_t* y,
+                        int64_t ldy, ql_stream_t stream) {
+  if (!y32 || !y) return QL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || ld32 < N || ldy < N) return QL_ERR_INVALID_ARG;
+  if (M > 65535 || N > (1 << 30)) return QL_ERR_UNSUPPORTED;
+  return cuda_status(launch_finish_f32(y32, (int)M, (int)N, ld32, bias, y, ldy, (cudaStream_t)stream));
 }
 
 // ------------------------------------------------------------------ shared skinny launcher (FP8 / MXFP4, bf16 act)
@@ -545,6 +623,41 @@ ql_status qlinear_fp8_block(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
   if (e != cudaSuccess) return cuda_status(e);
   if (path_out) *path_out = QL_PATH_FP8_TCGEN05;
   return QL_OK;
+}
+
+// a K shard of a row-parallel FP8-block layer: fp32 partial sums, bf16 activations
+ql_status qlinear_fp8_block_partial(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const uint8_t* w, int64_t N,
+                                    int64_t ldw, const uint8_t* w_scale, int block_n, int block_k, float* y32,
+                                    int64_t ldy32, void* workspace, size_t workspace_bytes, ql_stream_t stream,
+                                    int* path_out) {
+  if (path_out) *path_out = QL_PATH_NONE;
+  if (!x || !w || !w_scale || !y32) return QL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldx < K || ldw < K || ldy32 < N || block_n < 1 || block_k < 1)
+    return QL_ERR_INVALID_ARG;
+  if (M > 65535 || N > (1 << 30) || K > (1 << 30)) return QL_ERR_UNSUPPORTED;
+  if (K % 16 != 0 || cdiv(N, SK_ROWS) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
+  if (block_n % 16 != 0 || block_k % 64 != 0 || (block_k & (block_k - 1)) != 0) return QL_ERR_UNSUPPORTED;
+  if (!al16(x) || !al16(w) || ldx % 8 != 0 || ldw % 16 != 0) return QL_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < ql_workspace_bytes(QL_OP_FP8_BLOCK, M, N, K, 0, 0)) return QL_ERR_WORKSPACE;
+  if (!al16(workspace)) return QL_ERR_ALIGNMENT;
+  Dense2Call d = {};
+  d.fmt = FMT_FP8;
+  d.x = x;
+  d.M = M;
+  d.K = K;
+  d.ldx = ldx;
+  d.w = w;
+  d.N = N;
+  d.ldw = ldw;
+  d.wsb = w_scale;
+  d.lds = cdiv(K, block_k);
+  d.block_n = block_n;
+  d.block_k = block_k;
+  d.y32 = y32;
+  d.ldy32 = ldy32;
+  const ql_status s = run_dense2(d, workspace, (cudaStream_t)stream);
+  if (s == QL_OK && path_out) *path_out = QL_PATH_FP8_SKINNY;
+  return s;
 }
 
 // ------------------------------------------------------------------ FP8 per channel / per tensor
@@ -677,6 +790,37 @@ ql_status qlinear_mxfp4(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, co
 }
 
 // ------------------------------------------------------------------ MoE
+// a K shard of a row-parallel MXFP4 layer: fp32 partial sums, bf16 activations
+ql_status qlinear_mxfp4_partial(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const uint8_t* w, int64_t N,
+                                int64_t ldw_bytes, const uint8_t* w_scale, int64_t lds, float* y32, int64_t ldy32,
+                                void* workspace, size_t workspace_bytes, ql_stream_t stream, int* path_out) {
+  if (path_out) *path_out = QL_PATH_NONE;
+  if (!x || !w || !w_scale || !y32) return QL_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || ldx < K || ldw_bytes * 2 < K || lds * 32 < K || ldy32 < N) return QL_ERR_INVALID_ARG;
+  if (M > 65535 || N > (1 << 30) || K > (1 << 30)) return QL_ERR_UNSUPPORTED;
+  if (cdiv(N, SK_ROWS) > (int64_t)kMaxTickets) return QL_ERR_UNSUPPORTED;
+  if (!mxfp4_v2_ok(K, lds, w_scale)) return QL_ERR_UNSUPPORTED;  // whole 256-K units, 8-byte scale rows
+  if (!al16(x) || !al16(w) || ldx % 8 != 0 || ldw_bytes % 16 != 0) return QL_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < ql_workspace_bytes(QL_OP_MXFP4, M, N, K, 0, 0)) return QL_ERR_WORKSPACE;
+  if (!al16(workspace)) return QL_ERR_ALIGNMENT;
+  Dense2Call d = {};
+  d.fmt = FMT_MXFP4;
+  d.x = x;
+  d.M = M;
+  d.K = K;
+  d.ldx = ldx;
+  d.w = w;
+  d.N = N;
+  d.ldw = ldw_bytes;
+  d.wsb = w_scale;
+  d.lds = lds;
+  d.y32 = y32;
+  d.ldy32 = ldy32;
+  const ql_status s = run_dense2(d, workspace, (cudaStream_t)stream);
+  if (s == QL_OK && path_out) *path_out = QL_PATH_MXFP4_SKINNY;
+  return s;
+}
+
 ql_status moe_mxfp4_grouped(const uint16_t* x, int64_t M, int64_t H, const uint16_t* router_logits,
                             const int32_t* topk_ids_in, const float* topk_w_in, int E, int topk, int renormalize,
                             const uint8_t* w13, const uint8_t* s13, const uint8_t* w2, const uint8_t* s2, int64_t I,

@@ -68,7 +68,8 @@ struct I8Params {
 // written as exact f16 values into the image [M][kpad] (zeros past K) that the GEMM reads.
 __global__ void __launch_bounds__(256) quant_i8_image_kernel(const uint16_t* __restrict__ x, int K, int64_t ldx,
                                                              int kpad, uint16_t* __restrict__ img,
-                                                             float* __restrict__ xs, int8_t* xq_dbg, float* xs_dbg) {
+                                                             float* __restrict__ xs, int8_t* xq_dbg, float* xs_dbg,
+                                                             const float* __restrict__ amax_in) {
   pdl_launch_dependents();  // the GEMM may start and prefetch its weights
   const int m = blockIdx.x;
   const uint16_t* xr = x + (int64_t)m * ldx;
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(256) quant_i8_image_kernel(const uint16_t* __r
   __syncthreads();
   amax = fmaxf(fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3])),
                fmaxf(fmaxf(s_red[4], s_red[5]), fmaxf(s_red[6], s_red[7])));
+  if (amax_in) amax = amax_in[m];  // a K shard: the whole row's amax, from the caller
   const float s = __fdiv_rn(amax, 127.0f);
   uint16_t* ir = img + (int64_t)m * kpad;
   for (int k = threadIdx.x * 8; k < kpad; k += blockDim.x * 8) {
@@ -373,7 +375,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
     if (ok) {
       pdl_wait();  // x_s comes from the quantisation kernel
       if (n < p.N) {
-        const float ws = p.w_s[p.w_s_len > 1 ? n : 0];
+        const float ws = p.w_s ? p.w_s[p.w_s_len > 1 ? n : 0] : 0.f;
         const float bias = p.bias ? bf16_bits_to_f32(p.bias[n]) : 0.f;
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
@@ -381,6 +383,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
           if (c < half && t < p.M) {
             const int32_t a = sum[c];
             if (p.acc_out) p.acc_out[(int64_t)t * p.N + n] = a;
+            if (!p.y) continue;  // a K shard: the int32 sums are the result
             uint16_t yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)a, p.x_s[t]), ws));
             if (p.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + bias);
             p.y[(int64_t)t * p.ldy + n] = yb;
@@ -453,7 +456,7 @@ size_t i8_part_bytes(int64_t M, int64_t N, int64_t K) {
 cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st) {
   const int64_t kpad = i8_kpad(g.K);
   // activation codes (exact f16), per-token scales
-  quant_i8_image_kernel<<<g.M, 256, 0, st>>>(g.x, g.K, g.ldx, (int)kpad, g.img, g.xs, g.xq_dbg, g.xs_dbg);
+  quant_i8_image_kernel<<<g.M, 256, 0, st>>>(g.x, g.K, g.ldx, (int)kpad, g.img, g.xs, g.xq_dbg, g.xs_dbg, g.amax_in);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

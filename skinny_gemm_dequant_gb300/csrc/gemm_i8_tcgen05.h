@@ -17,7 +17,7 @@ struct I8GemmArgs {
   const float* w_s;  // fp32 [w_s_len], w_s_len = N or 1
   int w_s_len;
   const uint16_t* bias;  // bf16 [N] or null
-  uint16_t* y;           // bf16 [M, ldy]
+  uint16_t* y;           // bf16 [M, ldy], or null (a K shard: acc_out only)
   int64_t ldy;
   int32_t* acc_out;  // optional int32 [M, N]
   int8_t* xq_dbg;    // optional int8 [M, K]
@@ -28,6 +28,7 @@ struct I8GemmArgs {
   unsigned* tickets; // workspace: one arrival count per output tile, zero between calls
   uint32_t* status;
   uint32_t wait_limit;
+  const float* amax_in;  // optional fp32 [M]: per-token amax over the whole row (a K shard)
 };
 
 int64_t i8_kpad(int64_t K);

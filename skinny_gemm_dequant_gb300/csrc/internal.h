@@ -50,6 +50,9 @@ struct Skinny2Plan {
   size_t fp8_scale_bytes; // shared memory for the FP8 block-scale rows
 };
 Skinny2Plan skinny2_plan(int fmt, int64_t M, int64_t N, int64_t K, int block_n, int64_t slots = 1);
+// bytes at the start of every workspace that must be zero before a call (the status word, the
+// counters and the split-K tickets); the kernels leave them zero
+size_t workspace_zero_bytes();
 struct Skinny2Args;
 cudaError_t launch_skinny2(int fmt, const Skinny2Plan& p, const Skinny2Args& a, const uint8_t* w, int64_t ldw,
                            cudaStream_t st);
@@ -97,6 +100,13 @@ SplitK skinny_split(int fmt, int mt, int64_t row_blocks, int64_t K);
 size_t skinny_smem(int fmt, int mt, int kc);
 
 uint32_t wait_limit();
+
+// sharded-layer kernels (kernels_shard.cu)
+cudaError_t launch_token_amax(const uint16_t* x, int M, int K, int64_t ldx, float* amax, cudaStream_t st);
+cudaError_t launch_int8_epilogue(const int32_t* acc, int M, int N, const float* amax, const float* w_s, int w_s_len,
+                                 const uint16_t* bias, uint16_t* y, int64_t ldy, cudaStream_t st);
+cudaError_t launch_finish_f32(const float* y32, int M, int N, int64_t ld32, const uint16_t* bias, uint16_t* y,
+                              int64_t ldy, cudaStream_t st);
 
 // Raise a kernel's dynamic shared-memory limit to the device's opt-in maximum minus its static
 // shared memory.  Done once per kernel, before any launch, so calls made during CUDA-graph

@@ -15,12 +15,13 @@
 // little set-up work and should come before any stream capture.
 //
 // All calls on a device share the one array and it keeps whatever the previous call left
-// there: the part that must start at zero (the status word and the split-K tickets of this
-// call) is cleared on the caller's stream at the start of every call, and two calls that
+// there: the part that must start at zero (the status word, the counters and all split-K
+// tickets) is cleared on the caller's stream at the start of every call, and two calls that
 // overlap on the GPU (different streams, no ordering between them) race on the array.
 #include <mutex>
 
 #include "../../include/qlinear.h"
+#include "internal.h"
 #include <cuda_runtime.h>
 
 namespace {
@@ -63,8 +64,9 @@ extern "C" ql_status qlinear_int8_w8a8_noalloc(const uint16_t* x, int64_t M, int
   if (need == 0 || need > kScratchBytes) return QL_ERR_WORKSPACE;  // larger than the built-in scratch
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return QL_ERR_CUDA;
-  // status word (256 bytes) and one split-K ticket per 64-row block of this call
-  const size_t clear = 256 + 4 * (size_t)((N + 63) / 64);
+  // everything the kernels expect to find zero, whatever an earlier call (cut short by a
+  // timed-out wait, say) left behind
+  const size_t clear = ql::workspace_zero_bytes();
   if (cudaMemsetAsync(scratch, 0, clear, (cudaStream_t)stream) != cudaSuccess) return QL_ERR_CUDA;
   return qlinear_int8_w8a8(x, M, K, ldx, w, N, ldw, w_scale, w_scale_len, bias, y, ldy, acc_out, xq_out, xs_out,
                            scratch, kScratchBytes, stream, path_out);

@@ -105,7 +105,30 @@ struct Skinny2Args {
   uint32_t wait_limit;
   int stages;
   int xcopies;  // copies of the activation image; CTA c reads copy c % xcopies (spreads L2 load)
+  // INT8 dense layers of up to 4 tokens: every output is settled by the contribution that
+  // completes it (cells, see s2_cell_*)
+  unsigned long long* cells;  // [M][N]: (units added << 48) + exact int32 sum (zeroed by the jobs)
+  // K shards of a row-parallel layer: INT8 quantises with the caller's per-token amax (taken
+  // over the whole row) and may leave y null (acc_out only); FP8 / MXFP4 write fp32 partial
+  // sums to y32 (no bias) instead of bf16 y
+  const float* amax_in;
+  float* y32;
+  int64_t ldy32;
 };
+
+// A self-settling output cell of the INT8 kernel: a 64-bit word holding (units << 48) + s,
+// where s is the exact int32 sum of the partial dot products added so far (two's complement
+// across the word: |s| < 2^31 < 2^47).  Every contribution is one atomic add of
+// (n << 48) + partial, n = the units it covers, so the contribution whose add brings the count
+// to the row block's unit count holds the complete sum in the add's result, and settles the
+// output itself: no CTA waits for another, and the order of arrival cannot change the sum.
+__host__ __device__ __forceinline__ unsigned long long s2_cell_add(int units, int32_t partial) {
+  return ((unsigned long long)units << 48) + (unsigned long long)(long long)partial;
+}
+__host__ __device__ __forceinline__ int s2_cell_units(unsigned long long v) { return (int)((v + (1ull << 47)) >> 48); }
+__host__ __device__ __forceinline__ int32_t s2_cell_sum(unsigned long long v) {
+  return (int32_t)(long long)(v - ((unsigned long long)s2_cell_units(v) << 48));
+}
 
 template <int FMT>
 struct S2Traits {
@@ -242,6 +265,7 @@ __device__ void s2_prepare(const Skinny2Args& a, int m, int sl, int nsl, int tid
   float f, inv = 1.f;  // INT8: f = x_s and inv = RN(1/x_s); else f = 2^p and inv = 2^-p
   bool fast = true;    // INT8: x_s normal, so the reciprocal path is exact (see s2_code)
   if constexpr (FMT == FMT_INT8) {
+    if (a.amax_in) amax = a.amax_in[m];  // a K shard: the whole row's amax, from the caller
     f = __fdiv_rn(amax, 127.0f);
     fast = f >= 1.17549435e-38f;
     if (fast) inv = __frcp_rn(f);
@@ -297,6 +321,12 @@ __device__ void s2_prepare(const Skinny2Args& a, int m, int sl, int nsl, int tid
   if (sl == 0 && tid == 0) {
     a.tokf[m] = f;
     if (FMT == FMT_INT8 && a.xs_dbg) a.xs_dbg[m] = f;
+  }
+  if constexpr (FMT == FMT_INT8) {  // this slice of token m's output cells starts at zero
+    if (a.cells) {
+      const int r0 = (int)((int64_t)sl * a.N / nsl), r1 = (int)((int64_t)(sl + 1) * a.N / nsl);
+      for (int r = r0 + tid; r < r1; r += 256) a.cells[(int64_t)m * a.N + r] = 0ull;
+    }
   }
   consumer_sync();  // red[] is reused by the next job
 }
@@ -474,6 +504,23 @@ __device__ inline void s2_route(const Skinny2Args& a, int* s_ids, int* s_cnt, in
 // expert [E] int, count
 __host__ __device__ inline size_t s2_route_bytes(int P, int E) {
   return ((size_t)P * 4 + (size_t)(3 * E + 2) * 4 + 15) & ~size_t(15);
+}
+
+// the same load with an L2 cache policy (tc::l2_evict_*)
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* m, int x, int y, int z, int w,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, "
+      "%4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(tc::smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+// bring a box into L2 only (no shared memory, no barrier), under an L2 cache policy
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* m, int x, int y, int z, int w, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3, %4}], %5;" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+               : "memory");
 }
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, int x, int y, int z, int w,

@@ -38,6 +38,10 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
   constexpr bool kBF16 = (FMT == FMT_BF16);  // activations loaded as they are: no image, no jobs
   constexpr bool kF8C = (FMT == FMT_F8E4C || FMT == FMT_F8E5C);  // FP8 codes, one scale per channel
   constexpr bool kRowScale = kInt || kF8C;                         // fp32 w_scale applied once at the end
+  // INT8 dense layers of up to 8 tokens may settle their outputs through cells (exact integer
+  // sums, so neither the split nor the order of arrival can change a result); the host asks for
+  // it by passing the cells (a.cells)
+  constexpr bool kCellCode = kInt && !kMoE && MT == 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
@@ -45,12 +49,23 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
   uint64_t* empty = full + S;
   uint8_t* fp8sc = reinterpret_cast<uint8_t*>(empty + S);  // FP8 scale rows of this CTA's row blocks
   __shared__ int s_abort;
+  __shared__ int s_urb[8], s_ukt[8];  // kDyn: row block and K unit of the stage in each slot (-1: end)
 
   // the next kernel in the stream may launch now: it waits for this grid before it touches
   // memory, and meanwhile can take each SM this grid leaves and start streaming its weights
   pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, c = blockIdx.x;
+  if constexpr (!kBF16 && KIND != S2_MOE_DN) {
+    // the token rows this CTA's activation jobs will read, into L2 now, while the previous
+    // kernel may still run: the loads that use them come after the grid-dependency wait, and
+    // a write by the previous kernel lands in L2 all the same (a prefetch changes no value)
+    if (threadIdx.x == 0)
+      for (int j = c; j < a.M * s2_slices(a.M, G, kMoE ? 8 : 32); j += G)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.x + (int64_t)(j % a.M) * a.ldx),
+                     "r"((uint32_t)a.K * 2)
+                     : "memory");
+  }
   // the activation image: the consumer warps of CTAs c, c + G, ... each write one (row, slice)
   // job and count them in with one release (the rows are read by TMA, the async proxy, in other
   // CTAs: proxy fence first; the release is cumulative over the CTA's writes, ordered before it
@@ -96,6 +111,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
     }
   }
   const int64_t T = kMoE ? (int64_t)nu * a.nb * a.nk : a.total;
+  const bool kDyn = kCellCode && a.cells != nullptr;
   const int64_t s0 = (int64_t)c * T / G, s1 = (int64_t)(c + 1) * T / G;
   const int nk = a.nk;
   const uint32_t lim = a.wait_limit;
@@ -139,7 +155,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
     const int ksc = a.K / 32;  // MXFP4 scale bytes of a row that belong to K
     // the activation hand-off: wait (bounded) until the image is complete, count in (the last
     // producer returns both counters to zero for the next call) and report whether it timed out
-    auto handoff = [&]() {
+    auto handoff_wait = [&]() {
       pdl_wait();  // the counters belong to the previous call until its grid is done
       for (uint32_t n = 0;; ++n) {
         unsigned v;
@@ -152,13 +168,24 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
         __nanosleep(32);
       }
       asm volatile("fence.proxy.async.global;" ::: "memory");  // generic writes -> TMA reads
+    };
+    // counted in after the activation loads went out (its round trip is off the critical path)
+    auto handoff_count = [&]() {
       if (atomicAdd(a.done, 1u) == (unsigned)G - 1) {
         *a.ready = 0;
         *a.done = 0;
       }
     };
+    auto handoff = [&]() {
+      handoff_wait();
+      handoff_count();
+    };
     if (n_units == 0) {
       if (lane == 0 && !kBF16) handoff();
+      if (lane == 0 && kCellCode && kDyn) {  // the consumers wait for an end marker
+        s_urb[0] = -1;
+        tc::mbar_arrive(&full[0]);
+      }
       return;
     }
     // activation tiles of unit kt: the image (4D) or, for BF16, the caller's x itself (2D boxes
@@ -172,8 +199,70 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
         tma_load_4d(dst, &tmX, 0, xrow_, xcp, ktx * Tr::NXB, bar);
       }
     };
+    if (kCellCode && kDyn) {
+      // INT8 through the cells: this CTA's range, its first stages before the hand-off, each
+      // stage tagged with its row block and K unit for the consumers.  Lane 0 does all of it.
+      if (lane != 0) return;
+      const int pre_s = min(S, n_units);
+      const uint64_t wpol = tc::l2_evict_first();
+      bool ok = true;
+      int issued = 0, slot = 0;
+      uint32_t phase = 0;
+      int urb = rb_first, ukt = (int)(s0 - (int64_t)rb_first * nk);
+      for (int i = 0; i <= n_units; ++i) {
+        if (i >= S && !tc::mbar_wait(&empty[slot], phase ^ 1u, lim, abort)) {
+          fail();
+          ok = false;
+          break;
+        }
+        if (i == n_units) {  // no more units: tell the consumers
+          s_urb[slot] = -1;
+          tc::mbar_arrive(&full[slot]);
+          break;
+        }
+        s_urb[slot] = urb;
+        s_ukt[slot] = ukt;
+        const uint32_t st = tc::smem_u32(smem + (size_t)slot * STAGE);
+        tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + X_BYTES);
+        if (whole_chunks || (ukt + 1) * S2_WB <= a.wbytes) {
+          tma_load_4d_hint(st, &tmW, 0, urb * S2_ROWS, ukt * S2_CHUNKS, 0, &full[slot], wpol);
+        } else {
+          tc::tma_load_2d(smem + (size_t)slot * STAGE, &tmW2, ukt * S2_WB, urb * S2_ROWS, &full[slot]);
+          tc::tma_load_2d(smem + (size_t)slot * STAGE + W_CHUNK, &tmW2, ukt * S2_WB + 128, urb * S2_ROWS, &full[slot]);
+        }
+        if (i >= pre_s) {
+          load_x(st + W_BYTES, ukt, 0, &full[slot]);
+        } else if (i == pre_s - 1) {
+          // the stages so far went out without their activations: wait for the image, then
+          // load those
+          handoff_wait();
+          int kj = (int)(s0 - (int64_t)rb_first * nk);
+          for (int j = 0; j < pre_s; ++j) {
+            load_x(tc::smem_u32(smem + (size_t)j * STAGE) + W_BYTES, kj, 0, &full[j]);
+            if (++kj == nk) kj = 0;
+          }
+          handoff_count();
+        }
+        issued = i + 1;
+        if (++ukt == nk) {
+          ukt = 0;
+          ++urb;
+        }
+        if (++slot == S) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {  // no copy may land after the CTA exits
+        for (int i = max(0, issued - S); i < issued; ++i)
+          tc::mbar_wait(&full[i % S], (uint32_t)(i / S) & 1, 1u << 22, nullptr);
+      }
+      return;
+    }
     bool ok = true;
     int issued = 0;
+    // weights are read once: they leave L2 first, before activations, scales and outputs
+    const uint64_t wpol = tc::l2_evict_first();
     // unit counters kept incrementally: no divisions in the loop
     int rb = rb_first, kt = (int)(s0 - (int64_t)rb_first * nk);
     int u = kMoE ? rb / a.nb : 0, rbl = rb - u * a.nb;  // expert slot, block within the expert
@@ -195,7 +284,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
         // weights: chunks 2kt, 2kt+1 of rows rbl*128.. of expert ex -> smem [chunk][row][128 B]
         if (whole_chunks || (kt + 1) * S2_WB <= a.wbytes) {
           tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + X_BYTES);
-          tma_load_4d(st, &tmW, 0, rbl * S2_ROWS, kt * S2_CHUNKS, ex, &full[slot]);
+          tma_load_4d_hint(st, &tmW, 0, rbl * S2_ROWS, kt * S2_CHUNKS, ex, &full[slot], wpol);
         } else {
           // the row ends inside this unit, off a chunk boundary: a chunk at a time from the 2D
           // view, whose bytes past the end (a whole chunk, possibly) are filled with zeros
@@ -212,7 +301,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
           if constexpr (kBF16)
             pdl_wait();  // x may come from the previous kernel
           else
-            handoff();
+            handoff_wait();
           int ktj = (int)(s0 - (int64_t)rb_first * nk), rbj = rb_first;
           for (int j = 0; j < pre; ++j) {  // pre <= S: stage j is slot j
             const int uj = kMoE ? rbj / a.nb : 0;
@@ -223,6 +312,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
               ++rbj;
             }
           }
+          if constexpr (!kBF16) handoff_count();
         }
       }
       if constexpr (FMT == FMT_MXFP4) {
@@ -273,6 +363,138 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
   const int lrow = 16 * w + (lane & 7) + ((lane >> 3) & 1) * 8;
   const int lpc = lane >> 4;
 
+  if (kCellCode && kDyn) {
+    // INT8 units as the producer hands them over (slot -> row block, K unit).  A run of
+    // consecutive units of one row block is summed in registers (exact int32); when the run
+    // ends its sums go out as one atomic add per output cell (s2_cell_add), whose result is
+    // inspected at the end of the next run, so the round trip overlaps that run's work: the add
+    // that completed a cell's unit count settles the output, y = bf16((acc * x_s) * w_s) (+ bias
+    // after the cast).  The activation jobs zeroed the cells before the hand-off, and no stage
+    // reaches a consumer before it, so every cell starts the call at zero.
+    int32_t acci[MT][4];
+    unsigned long long pend[MT][4];  // cell values after this warp's last adds
+    int pend_rb = -1;                // their row block (-1: none outstanding)
+    int cur_rb = -1, last_kt = -2, run = 0;
+    const int row_g = 16 * w + g;
+    auto zero = [&]() {
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acci[m][r] = 0;
+    };
+    auto settle = [&]() {  // the outputs whose unit count the last adds completed
+      if (pend_rb < 0) return;
+      // the epilogue's factors first, so their loads overlap the adds' round trip
+      float xs[MT][2], wsr[2], bsr[2];
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int col = s2_rho(2 * t + e2) + 8 * m;
+          xs[m][e2] = col < a.M ? a.tokf[col] : 0.f;
+        }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = min(pend_rb * S2_ROWS + row_g + 8 * h, a.N - 1);
+        wsr[h] = a.w_scale ? a.w_scale[a.w_scale_len > 1 ? row : 0] : 0.f;
+        bsr[h] = a.bias ? bf16_bits_to_f32(a.bias[row]) : 0.f;
+      }
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int col = s2_rho(2 * t + (r & 1)) + 8 * m;
+          const int row = pend_rb * S2_ROWS + row_g + (r >= 2 ? 8 : 0);
+          if (row >= a.N || col >= a.M || s2_cell_units(pend[m][r]) != nk) continue;
+          const int32_t v = s2_cell_sum(pend[m][r]);
+          if (a.acc_out) a.acc_out[(int64_t)col * a.N + row] = v;
+          if (!a.y) continue;  // a K shard: the int32 sums are the result
+          uint16_t yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)v, xs[m][r & 1]), wsr[r >> 1]));
+          if (a.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + bsr[r >> 1]);
+          a.y[(int64_t)col * a.ldy + row] = yb;
+        }
+      pend_rb = -1;
+    };
+    auto post = [&]() {  // the run's sums to their cells
+      settle();
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int col = s2_rho(2 * t + (r & 1)) + 8 * m;
+          const int row = cur_rb * S2_ROWS + row_g + (r >= 2 ? 8 : 0);
+          if (row >= a.N || col >= a.M) continue;
+          const unsigned long long add = s2_cell_add(run, acci[m][r]);
+          pend[m][r] = atomicAdd(a.cells + (int64_t)col * a.N + row, add) + add;
+        }
+      pend_rb = cur_rb;
+      run = 0;
+      zero();
+    };
+    zero();
+    int slot = 0;
+    uint32_t phase = 0;
+    volatile int* vurb = s_urb;
+    volatile int* vukt = s_ukt;
+    while (true) {
+      int got = 0;
+      if (lane == 0) got = tc::mbar_wait(&full[slot], phase, lim, abort);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) {
+        if (lane == 0) fail();
+        return;  // the outputs of an aborted call are undefined (the status word says so)
+      }
+      const int urb = vurb[slot];
+      if (urb < 0) break;
+      const int ukt = vukt[slot];
+      if (run > 0 && (urb != cur_rb || ukt != last_kt + 1)) post();
+      cur_rb = urb;
+      last_kt = ukt;
+      const uint32_t st = tc::smem_u32(smem + (size_t)slot * STAGE);
+      const uint32_t xt = st + W_BYTES;
+      float ui[2][MT][4];  // two fp32 chains: integers below 2^24, exact
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) ui[e][m][0] = ui[e][m][1] = ui[e][m][2] = ui[e][m][3] = 0.f;
+#pragma unroll
+      for (int ck = 0; ck < S2_CHUNKS; ++ck) {
+        const uint32_t wt = st + ck * W_CHUNK;
+        uint32_t q[4][4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          ldmatrix_x4(wt + sw128(lrow, (2 * p + lpc) * 16), q[p][0], q[p][1], q[p][2], q[p][3]);
+#pragma unroll
+        for (int pc = 0; pc < 8; ++pc) {
+          const uint32_t qa = q[pc >> 1][2 * (pc & 1)], qb = q[pc >> 1][2 * (pc & 1) + 1];
+          uint32_t a0, a1, a2, a3;
+          s8x4_to_f16x2x2(qa, a0, a2);
+          s8x4_to_f16x2x2(qb, a1, a3);
+          const int kx = 16 * pc + 4 * t;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(gx + 8 * m, (kx & 63) * 2));
+            mma_f16_16816(ui[pc & 1][m], a0, a1, a2, a3, xv.x, xv.y);
+          }
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acci[m][r] += __float2int_rn(ui[0][m][r] + ui[1][m][r]);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&empty[slot]);
+      ++run;
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    if (run > 0) post();
+    settle();
+    return;
+  }
+
   // one complete row block's results (fp32 sums, or int32 bits for INT8) to their outputs.  The
   // per-token factors (x_s or 2^p) are read here: a stage has arrived by then, and activations
   // were loaded only after the image, factors included, was complete.
@@ -298,7 +520,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int row = min(row_w + g + 8 * e2, a.N - 1);
-        if (kRowScale) rowf[e2] = a.w_scale[a.w_scale_len > 1 ? row : 0];
+        if (kRowScale && a.w_scale) rowf[e2] = a.w_scale[a.w_scale_len > 1 ? row : 0];
         if (a.bias) rowb[e2] = bf16_bits_to_f32(a.bias[row]);
       }
     }
@@ -322,10 +544,15 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
           if constexpr (kInt) {
             const int32_t v = __float_as_int(res[m][r]);
             if (a.acc_out) a.acc_out[(int64_t)col * a.N + row] = v;
+            if (!a.y) continue;  // a K shard: the int32 sums are the result
             yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)v, colf[m][r & 1]), rowf[r >> 1]));
           } else if constexpr (kF8C) {
             yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn(res[m][r], colf[m][r & 1]), rowf[r >> 1]));
           } else {
+            if (a.y32) {  // a K shard: the fp32 partial sum, rounded once after the reduction
+              a.y32[(int64_t)col * a.ldy32 + row] = res[m][r] * colf[m][r & 1];
+              continue;
+            }
             yb = f32_to_bf16_rn(res[m][r] * colf[m][r & 1]);
           }
           if (a.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + rowb[r >> 1]);

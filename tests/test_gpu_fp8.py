@@ -78,6 +78,12 @@ def test_fp8_full_size_sampled(ql, N, K, M):
     compare(c, run(ql, c, K), K, rows=rows)
 
 
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)])
+def test_fp8_full_size_every_row(ql, N, K):
+    c = synth.fp8_block_case(4, N, K, seed=101)
+    compare(c, run(ql, c, K), K)
+
+
 def test_workspace_reuse_across_shapes(ql):
     """A small-N call with split-K partials, then a large-N call on the same workspace: every
     row of the second call must be right (the split-K tickets must not be disturbed)."""

@@ -83,6 +83,40 @@ def test_int8_full_size_sampled(ql, N, K, M):
     compare(c, run(ql, c), rows=rows)
 
 
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408), (10240, 5120)])
+@pytest.mark.parametrize("M", [4, 16])
+def test_int8_full_size_every_row(ql, N, K, M):
+    # every output row against the oracle: units are claimed at run time, so any row block
+    # may be split between CTAs in a different way on each call
+    c = synth.int8_case(M, N, K, seed=100 + M)
+    compare(c, run(ql, c))
+
+
+def _tie_tokens(K):
+    """Three tokens whose quotients x / x_s land exactly on half-integers: x_s = 1 (amax 127),
+    2 (amax 254) and 0.5 (amax 63.5), with x = x_s * (k + 1/2) in both signs."""
+    rows = []
+    for xs, amax in ((1.0, 127.0), (2.0, 254.0), (0.5, 63.5)):
+        half = np.arange(K - 1) % 127 + 0.5          # 0.5, 1.5, ..., 126.5
+        sign = np.where(np.arange(K - 1) % 2 == 0, 1.0, -1.0)
+        rows.append(np.concatenate([[amax], sign * half * xs]))
+    return synth.f32_to_bf16_bits(np.array(rows, np.float32))
+
+
+def test_int8_quantisation_ties_round_half_even(ql):
+    # the kernel's reciprocal product is exact here, so every code comes from the IEEE-quotient
+    # branch: rint must round each .5 to the even neighbour, as the oracle's does
+    K = 512
+    c = synth.int8_case(3, 256, K, seed=31)
+    c["x"] = _tie_tokens(K)
+    got = run(ql, c)
+    xq_ref, xs_ref = Q.quant_int8_per_token(c["x"])
+    assert xs_ref.tolist() == [1.0, 2.0, 0.5]
+    assert np.array_equal(got[2], xq_ref) and np.array_equal(got[3], xs_ref)
+    assert np.all(np.abs(xq_ref[:, 1:]) % 2 == 0)  # every tie went to an even code
+    compare(c, got)
+
+
 # ------------------------------------------------------------------ M > 16: the tcgen05 GEMM
 @pytest.mark.parametrize("M,N,K", [(17, 128, 256), (33, 200, 320), (64, 256, 1024), (100, 300, 640),
                                    (128, 130, 2048), (129, 64, 512), (200, 384, 1088), (256, 512, 4096)])
