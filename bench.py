@@ -61,7 +61,8 @@ WORKLOADS = {
           "(N,K)=(17408,5120), M in {64,128,256}",
     "n3": "MXFP4 MoE decode with clamped SwiGLU (alpha 1, limit 10): 256 experts, hidden 4096, "
           "intermediate 2048, top-8, M in 1..9",
-    "n1": "INT8 W8A8 GEMM on the tcgen05 path (per-token quantisation + kind::f16 MMAs on exact f16 images), "
+    "n1": "INT8 W8A8 for more than 16 tokens (M = 32: the persistent skinny kernel with four 8-token MMA tiles; "
+          "M > 32: per-token quantisation + tcgen05 kind::f16 MMAs on exact f16 images), "
           "27B-class shapes (N,K) in {(17408,5120),(5120,17408),(10240,5120)} x M in {32,64,128,256}",
     "n5": "Grouped MXFP4 MoE on the tcgen05 path with 1x128 E4M3 activations: 256 experts, hidden 4096, "
           "intermediate 2048, top-8, M in {32,64,128,256}",
@@ -116,7 +117,7 @@ _TC_SRC = ("gemm_tcgen05.cu", "gemm_tcgen05.h", "kernels_quant.cu", "quant_e4m3.
 _I8_SRC = ("gemm_i8_tcgen05.cu", "gemm_i8_tcgen05.h", "kernels_quant.cu", "tc_ptx.cuh", "common.cuh", "internal.h",
            "api.cu")
 KERNEL_SOURCES = {"c0": _SKINNY_SRC, "c1": _SKINNY_SRC, "c2": _SKINNY_SRC, "c3": _SKINNY_SRC, "c4": _TC_SRC,
-                  "n1": _I8_SRC, "n2": _SKINNY_SRC, "n3": _SKINNY_SRC, "n4": _SKINNY_SRC,
+                  "n1": tuple(dict.fromkeys(_I8_SRC + _SKINNY_SRC)), "n2": _SKINNY_SRC, "n3": _SKINNY_SRC, "n4": _SKINNY_SRC,
                   "n5": _TC_SRC + ("kernels_moe_grouped.cu", "route.cuh", "kernels_moe.cu")}
 
 
@@ -387,9 +388,10 @@ N1_MS = [32, 64, 128, 256]
 def build_n1(ql, torch):
     """INT8 W8A8 for M > 16 (a NEXT row): the tcgen05 GEMM, two launches per call."""
     w = build_c1(ql, torch, shapes=C1_SHAPES, Ms=N1_MS, name="n1")
-    w.launches_per_step = 2 * len(w.calls)  # quantisation + GEMM
+    # M <= 32: one skinny launch; above: quantisation + GEMM
+    w.launches_per_step = sum(1 if c["M"] <= 32 else 2 for c in w.calls)
     for c in w.calls:
-        c["kind"] = "int8_tcgen05"
+        c["kind"] = "int8_skinny" if c["M"] <= 32 else "int8_tcgen05"
     return w
 
 
@@ -439,7 +441,8 @@ KERNEL_DESC = {"c0": _SKINNY, "c1": _SKINNY, "c2": _SKINNY, "n2": _SKINNY, "n4":
                "n5": "grouped MoE launches per call (routing, dispatch, activation quantisation, two grouped "
                      "tcgen05 GEMMs, h quantisation, combine); bytes of the touched experts / event time per call",
                "c4": "tcgen05 block-scaled GEMM + its activation-quantisation launch; bytes / event time per call",
-               "n1": "INT8 tcgen05 GEMM + its per-token quantisation launch; bytes / event time per call"}
+               "n1": "INT8 for M > 16: skinny2_kernel (M = 32) or the tcgen05 GEMM + its per-token quantisation "
+                     "launch (M > 32); bytes / event time per call"}
 
 
 # ----------------------------------------------------------------------------- timing

@@ -95,8 +95,9 @@ QL_API int ql_version(void);
 
 /*
  * Bytes of workspace the op needs for these sizes.  Every layout starts with the same
- * 256 + 4*65536 bytes: the device status word, then the split-K tickets (kept at zero
- * between calls), so one workspace can serve calls of any op and shape in turn.  M, N, K as in the op; for
+ * 256 + 1 MiB: the device status word and counters, then a region that is zero between calls
+ * (split-K tickets, or the output cells of INT8 calls of up to 4 tokens), so one workspace can
+ * serve calls of any op and shape in turn.  M, N, K as in the op; for
  * QL_OP_MOE_MXFP4: M tokens, N = H (hidden), K = I (expert intermediate), E experts and
  * topk routed experts per token.  Returns 0 for an unknown op or negative sizes.
  */
@@ -130,8 +131,8 @@ QL_API void ql_set_wait_limit(uint32_t polls);
  * bias: nullable bf16 [N]; y: bf16 [M, ldy].
  * Debug outputs (nullable): acc_out int32 [M, N] (dense, ld N), xq_out int8 [M, K] (ld K),
  * xs_out fp32 [M].
- * Paths: M <= 16 -> the persistent skinny kernel (quantisation fused in, one launch);
- *        M > 16  -> a quantisation launch + the tcgen05 GEMM (kind::f16 MMAs on the exact f16
+ * Paths: M <= 32 -> the persistent skinny kernel (quantisation fused in, one launch);
+ *        M > 32  -> a quantisation launch + the tcgen05 GEMM (kind::f16 MMAs on the exact f16
  *                   values of the codes and weights, drained to int32 every 512 K).
  * Requires: M >= 1, N >= 1, K >= 16, K % 16 == 0, ldx >= K, ldw >= K, ldw % 16 == 0,
  * ldy >= N, 16-byte aligned x and w, |acc| < 2^31 (always true for K <= 133152).

@@ -14,6 +14,9 @@ using namespace ql;
 #ifndef QL_CELL_TOKENS
 #define QL_CELL_TOKENS 4
 #endif
+#ifndef QL_LOCAL_MK
+#define QL_LOCAL_MK 40960
+#endif
 
 namespace {
 
@@ -29,14 +32,26 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // no call's data region ever overlaps them (the kernels return every counter and ticket to
 // zero); op regions follow, carved in order.
 constexpr size_t kMaxTickets = 65536;
+// the region after the status word that is zero between calls: the split-K tickets (first
+// 4*kMaxTickets bytes) or, for INT8 calls of up to kCellTokens tokens, their output cells
+// (those calls use no tickets); the kernels leave it zero
+constexpr size_t kZeroRegion = size_t(1) << 20;
 constexpr size_t kReadyOff = 32, kDoneOff = 36;
 // INT8 calls of up to this many tokens settle their outputs through atomic cells (skinny2.cuh,
 // s2_cell_*); larger ones through per-CTA partial sums and a waiting settler.  Measured on the
 // INT8 decode bench: cells are faster at 1..4 tokens (most at N = 5120, K = 17408, where a row
 // block is shared by about 8 CTAs), slower at 8 and 16 (their atomic traffic grows with M)
 constexpr int64_t kCellTokens = QL_CELL_TOKENS;
+// tokens one launch of the persistent skinny kernel takes: up to 32 for INT8 (four 8-token MMA
+// tiles), 16 for the other formats; more tokens run in chunks (INT8: the tcgen05 GEMM)
+constexpr int64_t kSkinnyMaxTokens = 32;
+inline int64_t skinny_tokens(int fmt) { return fmt == FMT_INT8 ? kSkinnyMaxTokens : 16; }
+// dense layers whose M * K is at most this build their activation image inside every CTA
+// (each CTA reads the tokens' whole rows, so the cost grows with M * K) instead of sharing one
+// through global memory, which takes a grid-wide hand-off per call
+constexpr int64_t kLocalMK = QL_LOCAL_MK;
 constexpr size_t kTicketOff = 256;
-constexpr size_t kRegionsOff = kTicketOff + 4 * kMaxTickets;
+constexpr size_t kRegionsOff = kTicketOff + kZeroRegion;
 
 struct Carver {
   size_t off = kRegionsOff;
@@ -92,6 +107,7 @@ DenseLayout dense_layout(int fmt, int64_t M, int64_t N, int64_t K) {
 struct Dense2Layout {
   Skinny2Plan p;
   size_t cells, x16, sc, part, total;
+  bool cells_clean;  // the cells sit in the zero region (left zero by the kernel)
 };
 
 Dense2Layout dense2_layout(int fmt, int64_t Mc, int64_t N, int64_t K, int block_n) {
@@ -99,10 +115,13 @@ Dense2Layout dense2_layout(int fmt, int64_t Mc, int64_t N, int64_t K, int block_
   l.p = skinny2_plan(fmt, Mc, N, K, block_n);
   Carver c;
   const bool cells = fmt == FMT_INT8 && Mc <= kCellTokens;
-  l.cells = c.take(cells ? (size_t)N * Mc * 8 : 0);  // INT8 output cells [M][N]
+  // INT8 output cells [M][N]: in the zero region when they fit (no zeroing inside the call),
+  // else in a region of their own that the call's activation jobs zero first
+  l.cells_clean = cells && (size_t)N * Mc * 8 <= kZeroRegion;
+  l.cells = l.cells_clean ? kTicketOff : c.take(cells ? (size_t)N * Mc * 8 : 0);
   l.x16 = c.take((size_t)kXCopies * Mc * l.p.kpad * 2);
-  l.sc = c.take(16 * 4);
-  l.part = c.take(cells ? 0 : (size_t)l.p.grid * 16 * S2_ROWS * 4);  // one partial slot per CTA
+  l.sc = c.take(kSkinnyMaxTokens * 4);
+  l.part = c.take(cells ? 0 : (size_t)l.p.grid * l.p.mp * S2_ROWS * 4);  // one partial slot per CTA
   l.total = c.off;
   return l;
 }
@@ -277,8 +296,9 @@ size_t ql::workspace_zero_bytes() { return kRegionsOff; }
 
 namespace {
 ql_status run_dense2(const Dense2Call& d, void* workspace, cudaStream_t st) {
-  for (int64_t m0 = 0; m0 < d.M; m0 += 16) {
-    const int64_t Mc = (d.M - m0) < 16 ? (d.M - m0) : 16;
+  const int64_t chunk = skinny_tokens(d.fmt);
+  for (int64_t m0 = 0; m0 < d.M; m0 += chunk) {
+    const int64_t Mc = (d.M - m0) < chunk ? (d.M - m0) : chunk;
     const Dense2Layout l = dense2_layout(d.fmt, Mc, d.N, d.K, d.block_n);
     Skinny2Args a = {};
     a.M = (int)Mc;
@@ -309,6 +329,9 @@ ql_status run_dense2(const Dense2Call& d, void* workspace, cudaStream_t st) {
     a.part = at<float>(workspace, l.part);
     a.tickets = at<unsigned>(workspace, kTicketOff);
     a.cells = (d.fmt == FMT_INT8 && Mc <= kCellTokens) ? at<unsigned long long>(workspace, l.cells) : nullptr;
+    a.cells_clean = l.cells_clean ? 1 : 0;
+    // local activations: no activation jobs run, so INT8 cells must already be clean
+    a.local = (d.fmt != FMT_BF16 && Mc * d.K <= kLocalMK && (a.cells == nullptr || a.cells_clean)) ? 1 : 0;
     a.status = at<uint32_t>(workspace, 0);
     a.wait_limit = g_wait_limit;
     const cudaError_t e = launch_skinny2(d.fmt, l.p, a, d.w, d.ldw, st);
@@ -342,8 +365,9 @@ size_t ql_workspace_bytes(int op, int64_t M, int64_t N, int64_t K, int E, int to
   const int64_t Mc = M < 16 ? M : 16;  // skinny kernels run 16 tokens at a time
   switch (op) {
     case QL_OP_INT8_W8A8: {
-      const size_t a = dense2_layout(FMT_INT8, Mc, N, K, 128).total;
-      const size_t b = M > 16 ? i8_layout(M, N, K).total : 0;
+      const int64_t Mi = M < kSkinnyMaxTokens ? M : kSkinnyMaxTokens;
+      const size_t a = dense2_layout(FMT_INT8, Mi, N, K, 128).total;
+      const size_t b = M > kSkinnyMaxTokens ? i8_layout(M, N, K).total : 0;
       return a > b ? a : b;
     }
     case QL_OP_FP8_BLOCK: {
@@ -412,7 +436,7 @@ ql_status int8_impl(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, const 
   if (!al16(workspace)) return QL_ERR_ALIGNMENT;
   cudaStream_t st = (cudaStream_t)stream;
 
-  if (M > 16) {
+  if (M > kSkinnyMaxTokens) {
     // prefill-sized batches: one GEMM on the tensor cores streams the weights once
     const I8Layout l = i8_layout(M, N, K);
     tc::I8GemmArgs g = {};

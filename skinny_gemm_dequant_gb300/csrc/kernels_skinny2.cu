@@ -16,7 +16,7 @@ namespace ql {
 // device knows the actual count and splits the units by it)
 Skinny2Plan skinny2_plan(int fmt, int64_t M, int64_t N, int64_t K, int block_n, int64_t slots) {
   Skinny2Plan p;
-  p.mt = M <= 8 ? 1 : 2;
+  p.mt = M <= 8 ? 1 : (M <= 16 ? 2 : 4);  // 8-token MMA tiles (4: INT8 only)
   p.mp = 8 * p.mt;
   const int kpu = fmt == FMT_MXFP4 ? S2Traits<FMT_MXFP4>::KPU
                                    : (fmt == FMT_BF16 ? S2Traits<FMT_BF16>::KPU : S2Traits<FMT_INT8>::KPU);  // K per unit
@@ -96,6 +96,22 @@ static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w
   int S = (int)((optin - fixed) / (STAGE + 16));
   if (S > 8) S = 8;
   if (S < 2) return cudaErrorInvalidValue;
+  // local activations: weight-only stages plus the CTA's image of its own K units; taken only
+  // when the ring keeps at least the depth of the shared-image layout
+  size_t local_bytes = 0;
+  uint32_t stage_bytes = STAGE;
+  if (KIND == S2_DENSE_LOCAL) {
+    const int64_t slots = p.units_per_cta < p.nk ? p.units_per_cta : p.nk;
+    const size_t lb = ((size_t)slots * Tr::NXB * a.M * 128 + 127) & ~size_t(127);
+    const uint32_t sb = S2_ROWS * S2_WB + Tr::SCB;
+    int SL = (optin > (int)(fixed + lb)) ? (int)((optin - fixed - lb) / (sb + 16)) : 0;
+    if (SL > 8) SL = 8;
+    if (SL < S || SL < 3) return cudaErrorNotSupported;  // the caller takes the shared image
+    S = SL;
+    local_bytes = lb;
+    stage_bytes = sb;
+  }
+  a.local_bytes = (int)local_bytes;
   a.stages = S;
   a.bk_shift = 0;
   while (a.block_k > 0 && (1 << a.bk_shift) < a.block_k) ++a.bk_shift;
@@ -104,7 +120,7 @@ static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w
   a.total = p.total;
   const uint64_t wbytes = FMT == FMT_MXFP4 ? (uint64_t)a.K / 2 : (FMT == FMT_BF16 ? (uint64_t)a.K * 2 : (uint64_t)a.K);
   a.wbytes = (int)wbytes;
-  const size_t smem = 1024 + (size_t)S * STAGE + (size_t)S * 16 + extra;
+  const size_t smem = 1024 + (size_t)S * stage_bytes + (size_t)S * 16 + local_bytes + extra;
   CUtensorMap tw, tw2, tx;
   // whole 128-byte chunks as the third dimension (a box of 2 chunks is one 32 KB TMA operation),
   // experts as the fourth
@@ -155,9 +171,20 @@ static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w
 cudaError_t launch_skinny2(int fmt, const Skinny2Plan& p, const Skinny2Args& a, const uint8_t* w, int64_t ldw,
                            cudaStream_t st) {
   const int64_t es = (int64_t)a.N * ldw;  // one expert
+  if (a.local && p.mt == 1 && fmt != FMT_BF16) {
+    // every CTA builds its own activation image, when the ring keeps its depth beside it
+    cudaError_t e = cudaErrorNotSupported;
+    if (fmt == FMT_INT8) e = launch2<FMT_INT8, 1, S2_DENSE_LOCAL>(p, a, w, ldw, es, 1, st);
+    else if (fmt == FMT_FP8) e = launch2<FMT_FP8, 1, S2_DENSE_LOCAL>(p, a, w, ldw, es, 1, st);
+    else if (fmt == FMT_F8E4C) e = launch2<FMT_F8E4C, 1, S2_DENSE_LOCAL>(p, a, w, ldw, es, 1, st);
+    else if (fmt == FMT_F8E5C) e = launch2<FMT_F8E5C, 1, S2_DENSE_LOCAL>(p, a, w, ldw, es, 1, st);
+    else if (fmt == FMT_MXFP4) e = launch2<FMT_MXFP4, 1, S2_DENSE_LOCAL>(p, a, w, ldw, es, 1, st);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (fmt == FMT_INT8)
-    return p.mt == 1 ? launch2<FMT_INT8, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
-                     : launch2<FMT_INT8, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);
+    return p.mt == 1   ? launch2<FMT_INT8, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
+           : p.mt == 2 ? launch2<FMT_INT8, 2, S2_DENSE>(p, a, w, ldw, es, 1, st)
+                       : launch2<FMT_INT8, 4, S2_DENSE>(p, a, w, ldw, es, 1, st);
   if (fmt == FMT_FP8)
     return p.mt == 1 ? launch2<FMT_FP8, 1, S2_DENSE>(p, a, w, ldw, es, 1, st)
                      : launch2<FMT_FP8, 2, S2_DENSE>(p, a, w, ldw, es, 1, st);

@@ -46,7 +46,8 @@ constexpr int S2_CHUNKS = 2;                // 128-byte K chunks per unit
 constexpr int S2_WB = 128 * S2_CHUNKS;      // weight bytes per row per unit
 
 // what one launch computes: a dense linear layer, or one of the two expert GEMVs of the MoE
-enum { S2_DENSE = 0, S2_MOE_GU = 1, S2_MOE_DN = 2 };
+// (S2_DENSE_LOCAL: a dense layer whose CTAs build their own activation image, s2_local_image)
+enum { S2_DENSE = 0, S2_MOE_GU = 1, S2_MOE_DN = 2, S2_DENSE_LOCAL = 3 };
 
 struct Skinny2Args {
   int M, N, K;     // N: weight rows (per expert for the MoE kinds); M: tokens
@@ -107,13 +108,19 @@ struct Skinny2Args {
   int xcopies;  // copies of the activation image; CTA c reads copy c % xcopies (spreads L2 load)
   // INT8 dense layers of up to 4 tokens: every output is settled by the contribution that
   // completes it (cells, see s2_cell_*)
-  unsigned long long* cells;  // [M][N]: (units added << 48) + exact int32 sum (zeroed by the jobs)
+  unsigned long long* cells;  // [M][N]: (units added << 48) + exact int32 sum
+  int cells_clean;            // 1: the cells start at zero and each is reset after it settles;
+                              // 0: the activation jobs zero them before the hand-off
   // K shards of a row-parallel layer: INT8 quantises with the caller's per-token amax (taken
   // over the whole row) and may leave y null (acc_out only); FP8 / MXFP4 write fp32 partial
   // sums to y32 (no bias) instead of bf16 y
   const float* amax_in;
   float* y32;
   int64_t ldy32;
+  // dense layers with few tokens: each CTA builds the image of its own units in shared memory
+  // (s2_local_image, launch kind S2_DENSE_LOCAL) instead of the grid sharing one in global memory
+  int local;        // the host asks for it
+  int local_bytes;  // shared memory of the local image (behind the ring's barriers)
 };
 
 // A self-settling output cell of the INT8 kernel: a 64-bit word holding (units << 48) + s,
@@ -226,6 +233,56 @@ __device__ __forceinline__ float s2_code(float xv, float s, float r) {
   return fminf(fmaxf(rintf(y), -127.f), 127.f);
 }
 
+// The per-token factors of the activation image from the token's amax.  INT8: f = x_s =
+// amax / 127 (IEEE division) and inv = RN(1/x_s), fast when x_s is normal (see s2_code).
+// bf16 paths: f = 2^p and inv = 2^-p with p from the amax's exponent (scaled amax in
+// [2^14, 2^15)).
+template <int FMT>
+__device__ __forceinline__ void s2_token_factors(float amax, float& f, float& inv, bool& fast) {
+  inv = 1.f;
+  fast = true;
+  if constexpr (FMT == FMT_INT8) {
+    f = __fdiv_rn(amax, 127.0f);
+    fast = f >= 1.17549435e-38f;
+    if (fast) inv = __frcp_rn(f);
+  } else {
+    int p = 0;
+    if (amax > 0.f) p = max((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127, -126) - 14;
+    p = max(-100, min(100, p));
+    f = __uint_as_float((uint32_t)(127 + p) << 23);
+    inv = __uint_as_float((uint32_t)(127 - p) << 23);
+  }
+}
+
+// Eight bf16 values (one 16-byte vector) to their four f16x2 image words: INT8 codes
+// clamp(rint(x / x_s), -127, 127) as exact f16 integers (qb: the codes as bytes), or x * 2^-p.
+template <int FMT>
+__device__ __forceinline__ void s2_conv8(const uint4 u, float f, float inv, bool fast, uint32_t (&h)[4],
+                                         uint32_t (&qb)[2]) {
+  const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+  qb[0] = qb[1] = 0u;
+  if constexpr (FMT == FMT_INT8) {
+    float qv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float xv = (e & 1) ? __uint_as_float(wv[e >> 1] & 0xFFFF0000u) : __uint_as_float(wv[e >> 1] << 16);
+      float q = 0.f;
+      if (fast)
+        q = s2_code(xv, f, inv);
+      else if (f > 0.f)
+        q = fminf(fmaxf(rintf(__fdiv_rn(xv, f)), -127.f), 127.f);
+      qv[e] = q;
+      qb[e >> 2] |= ((uint32_t)((int)q & 0xFF)) << (8 * (e & 3));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) h[j] = pack_f16x2(qv[2 * j], qv[2 * j + 1]);  // exact: |q| <= 127
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      h[j] = pack_f16x2(__uint_as_float(wv[j] << 16) * inv, __uint_as_float(wv[j] & 0xFFFF0000u) * inv);
+  }
+}
+
 // Activation image, one job = (token m, slice sl of nsl): the 256 consumer threads of a CTA
 // (thread tid) find the token's amax over all of K, then write their slice of the row into
 // every copy of the image.  INT8: dynamic per-token quantisation, x_s = amax/127 and codes
@@ -262,47 +319,16 @@ __device__ void s2_prepare(const Skinny2Args& a, int m, int sl, int nsl, int tid
   if ((tid & 31) == 0) red[tid >> 5] = amax;
   consumer_sync();
   amax = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])), fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7])));
-  float f, inv = 1.f;  // INT8: f = x_s and inv = RN(1/x_s); else f = 2^p and inv = 2^-p
-  bool fast = true;    // INT8: x_s normal, so the reciprocal path is exact (see s2_code)
-  if constexpr (FMT == FMT_INT8) {
-    if (a.amax_in) amax = a.amax_in[m];  // a K shard: the whole row's amax, from the caller
-    f = __fdiv_rn(amax, 127.0f);
-    fast = f >= 1.17549435e-38f;
-    if (fast) inv = __frcp_rn(f);
-  } else {
-    int p = 0;
-    if (amax > 0.f) p = max((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127, -126) - 14;
-    p = max(-100, min(100, p));
-    f = __uint_as_float((uint32_t)(127 + p) << 23);
-    inv = __uint_as_float((uint32_t)(127 - p) << 23);
-  }
+  if (FMT == FMT_INT8 && a.amax_in) amax = a.amax_in[m];  // a K shard: the whole row's amax, from the caller
+  float f, inv;  // INT8: f = x_s and inv = RN(1/x_s); else f = 2^p and inv = 2^-p
+  bool fast;     // INT8: x_s normal, so the reciprocal path is exact (see s2_code)
+  s2_token_factors<FMT>(amax, f, inv, fast);
   const int64_t cstride = (int64_t)a.img_rows * a.kpad;  // elements between copies
   uint16_t* out = a.x16 + (int64_t)m * a.kpad;
   auto conv = [&](const uint4 u, int i) {
-    const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-    uint32_t h[4];
-    if constexpr (FMT == FMT_INT8) {
-      float qv[8];
-      uint32_t qb[2] = {0u, 0u};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float xv = (e & 1) ? __uint_as_float(wv[e >> 1] & 0xFFFF0000u) : __uint_as_float(wv[e >> 1] << 16);
-        float q = 0.f;
-        if (fast)
-          q = s2_code(xv, f, inv);
-        else if (f > 0.f)
-          q = fminf(fmaxf(rintf(__fdiv_rn(xv, f)), -127.f), 127.f);
-        qv[e] = q;
-        qb[e >> 2] |= ((uint32_t)((int)q & 0xFF)) << (8 * (e & 3));
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) h[j] = pack_f16x2(qv[2 * j], qv[2 * j + 1]);  // exact: |q| <= 127
-      if (a.xq_dbg) *reinterpret_cast<uint2*>(a.xq_dbg + (int64_t)m * a.K + 8 * i) = make_uint2(qb[0], qb[1]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        h[j] = pack_f16x2(__uint_as_float(wv[j] << 16) * inv, __uint_as_float(wv[j] & 0xFFFF0000u) * inv);
-    }
+    uint32_t h[4], qb[2];
+    s2_conv8<FMT>(u, f, inv, fast, h, qb);
+    if (FMT == FMT_INT8 && a.xq_dbg) *reinterpret_cast<uint2*>(a.xq_dbg + (int64_t)m * a.K + 8 * i) = make_uint2(qb[0], qb[1]);
     const uint4 hv = make_uint4(h[0], h[1], h[2], h[3]);
     for (int cp = 0; cp < a.xcopies; ++cp) *reinterpret_cast<uint4*>(out + cp * cstride + 8 * i) = hv;
   };
@@ -323,12 +349,71 @@ __device__ void s2_prepare(const Skinny2Args& a, int m, int sl, int nsl, int tid
     if (FMT == FMT_INT8 && a.xs_dbg) a.xs_dbg[m] = f;
   }
   if constexpr (FMT == FMT_INT8) {  // this slice of token m's output cells starts at zero
-    if (a.cells) {
+    if (a.cells && !a.cells_clean) {
       const int r0 = (int)((int64_t)sl * a.N / nsl), r1 = (int)((int64_t)(sl + 1) * a.N / nsl);
       for (int r = r0 + tid; r < r1; r += 256) a.cells[(int64_t)m * a.N + r] = 0ull;
     }
   }
   consumer_sync();  // red[] is reused by the next job
+}
+
+// The local activation image of a CTA (dense layers with few tokens, a.local): the CTA reads
+// its tokens' whole rows for their amax, then writes the image values of the K units it
+// streams into shared memory - no image in global memory, no hand-off between CTAs.  The
+// CTA's units are n_slots consecutive K units starting at kt0 (wrapping at nk); slot s holds
+// unit kt0 + s as NXB slabs of 64 K, each slab M rows of 128 bytes with the 128-byte swizzle
+// of a TMA tile (the consumers address it the same way, with row indices clamped to M - 1).
+// Also writes the tokens' factors to tokf (shared), the INT8 codes of those units to xq_dbg
+// and, in CTA 0, the INT8 x_s to xs_dbg.  All 256 consumer threads call this.
+template <int FMT>
+__device__ void s2_local_image(const Skinny2Args& a, uint32_t L, int kt0, int n_slots, int tid, float* red,
+                               float* tokf) {
+  constexpr int KPU = S2Traits<FMT>::KPU, VPU = KPU / 8;  // 8-element vectors per unit
+  const int nvec = a.K / 8, M = a.M;
+  const uint32_t slot_bytes = (uint32_t)(S2Traits<FMT>::NXB * M * 128);
+  __shared__ float s_inv[16];
+  __shared__ int s_fast[16];
+  for (int m = 0; m < M; ++m) {
+    const uint16_t* xr = a.x + (int64_t)m * a.ldx;
+    float amax = 0.f;
+    for (int i = tid; i < nvec; i += 256) {
+      const uint4 u = *reinterpret_cast<const uint4*>(xr + 8 * i);
+      amax = fmaxf(amax, fmaxf(fmaxf(bf16x2_absmax(u.x), bf16x2_absmax(u.y)), fmaxf(bf16x2_absmax(u.z), bf16x2_absmax(u.w))));
+    }
+    amax = warp_max(amax);
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    consumer_sync();
+    if (tid == 0) {
+      amax = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])), fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7])));
+      if (FMT == FMT_INT8 && a.amax_in) amax = a.amax_in[m];  // a K shard: the whole row's amax
+      float f, inv;
+      bool fast;
+      s2_token_factors<FMT>(amax, f, inv, fast);
+      tokf[m] = f;
+      s_inv[m] = inv;
+      s_fast[m] = fast;
+      if (FMT == FMT_INT8 && a.xs_dbg && blockIdx.x == 0) a.xs_dbg[m] = f;
+    }
+    consumer_sync();  // red[] is reused by the next token
+  }
+  const int total = n_slots * VPU * M;
+  for (int v = tid; v < total; v += 256) {
+    const int m = v % M, rest = v / M;
+    const int sl = rest / VPU, c8 = rest - sl * VPU;
+    int kt = kt0 + sl;
+    if (kt >= a.nk) kt -= a.nk;
+    const int k = kt * KPU + c8 * 8;
+    const uint4 u = k < a.K ? *reinterpret_cast<const uint4*>(a.x + (int64_t)m * a.ldx + k) : make_uint4(0, 0, 0, 0);
+    uint32_t h[4], qb[2];
+    s2_conv8<FMT>(u, tokf[m], s_inv[m], s_fast[m] != 0, h, qb);
+    if (FMT == FMT_INT8 && a.xq_dbg && k < a.K)
+      *reinterpret_cast<uint2*>(a.xq_dbg + (int64_t)m * a.K + k) = make_uint2(qb[0], qb[1]);
+    const int j = c8 >> 3, c16 = c8 & 7;  // slab, 16-byte chunk of the 128-byte row
+    const uint32_t dst = L + (uint32_t)sl * slot_bytes + (uint32_t)(j * M + m) * 128u + (uint32_t)((c16 ^ (m & 7)) << 4);
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                 : "memory");
+  }
+  consumer_sync();
 }
 
 // MoE down activations, one job = (dispatch position q, slice sl of nsl).  The pair p = m*topk+j

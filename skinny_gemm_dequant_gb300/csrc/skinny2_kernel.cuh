@@ -34,7 +34,10 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
   constexpr uint32_t X_BYTES = Tr::NXB * X_BOX;
   constexpr uint32_t STAGE = s2_stage_bytes<FMT, MT>();
   constexpr bool kInt = (FMT == FMT_INT8);
-  constexpr bool kMoE = (KIND != S2_DENSE);
+  constexpr bool kMoE = (KIND == S2_MOE_GU || KIND == S2_MOE_DN);
+  // local activations (dense layers with few tokens): stages carry weights only and every CTA
+  // builds the activation image of its own units behind the barriers (s2_local_image)
+  constexpr bool kLocal = (KIND == S2_DENSE_LOCAL);
   constexpr bool kBF16 = (FMT == FMT_BF16);  // activations loaded as they are: no image, no jobs
   constexpr bool kF8C = (FMT == FMT_F8E4C || FMT == FMT_F8E5C);  // FP8 codes, one scale per channel
   constexpr bool kRowScale = kInt || kF8C;                         // fp32 w_scale applied once at the end
@@ -45,11 +48,16 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * STAGE);
+  constexpr bool loc = kLocal;
+  constexpr uint32_t XB = loc ? 0u : X_BYTES;                 // activation bytes of a stage
+  constexpr uint32_t STB = loc ? W_BYTES + Tr::SCB : STAGE;   // stage stride (a multiple of 1 KB)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * STB);
   uint64_t* empty = full + S;
-  uint8_t* fp8sc = reinterpret_cast<uint8_t*>(empty + S);  // FP8 scale rows of this CTA's row blocks
+  uint8_t* limg = reinterpret_cast<uint8_t*>(empty + S);  // local activation image (a.local_bytes)
+  uint8_t* fp8sc = limg + a.local_bytes;  // FP8 scale rows of this CTA's row blocks
   __shared__ int s_abort;
   __shared__ int s_urb[8], s_ukt[8];  // kDyn: row block and K unit of the stage in each slot (-1: end)
+  __shared__ float s_tokf[Mp];         // local activations: the tokens' factors
 
   // the next kernel in the stream may launch now: it waits for this grid before it touches
   // memory, and meanwhile can take each SM this grid leaves and start streaming its weights
@@ -60,8 +68,9 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
     // the token rows this CTA's activation jobs will read, into L2 now, while the previous
     // kernel may still run: the loads that use them come after the grid-dependency wait, and
     // a write by the previous kernel lands in L2 all the same (a prefetch changes no value)
+    // (local activations: every CTA reads every row)
     if (threadIdx.x == 0)
-      for (int j = c; j < a.M * s2_slices(a.M, G, kMoE ? 8 : 32); j += G)
+      for (int j = kLocal ? 0 : c; j < (kLocal ? a.M : a.M * s2_slices(a.M, G, kMoE ? 8 : 32)); j += kLocal ? 1 : G)
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.x + (int64_t)(j % a.M) * a.ldx),
                      "r"((uint32_t)a.K * 2)
                      : "memory");
@@ -181,7 +190,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
       handoff_count();
     };
     if (n_units == 0) {
-      if (lane == 0 && !kBF16) handoff();
+      if (lane == 0 && !kBF16 && !loc) handoff();
       if (lane == 0 && kCellCode && kDyn) {  // the consumers wait for an end marker
         s_urb[0] = -1;
         tc::mbar_arrive(&full[0]);
@@ -222,15 +231,17 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
         }
         s_urb[slot] = urb;
         s_ukt[slot] = ukt;
-        const uint32_t st = tc::smem_u32(smem + (size_t)slot * STAGE);
-        tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + X_BYTES);
+        const uint32_t st = tc::smem_u32(smem + (size_t)slot * STB);
+        tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + XB);
         if (whole_chunks || (ukt + 1) * S2_WB <= a.wbytes) {
           tma_load_4d_hint(st, &tmW, 0, urb * S2_ROWS, ukt * S2_CHUNKS, 0, &full[slot], wpol);
         } else {
-          tc::tma_load_2d(smem + (size_t)slot * STAGE, &tmW2, ukt * S2_WB, urb * S2_ROWS, &full[slot]);
-          tc::tma_load_2d(smem + (size_t)slot * STAGE + W_CHUNK, &tmW2, ukt * S2_WB + 128, urb * S2_ROWS, &full[slot]);
+          tc::tma_load_2d(smem + (size_t)slot * STB, &tmW2, ukt * S2_WB, urb * S2_ROWS, &full[slot]);
+          tc::tma_load_2d(smem + (size_t)slot * STB + W_CHUNK, &tmW2, ukt * S2_WB + 128, urb * S2_ROWS, &full[slot]);
         }
-        if (i >= pre_s) {
+        if (loc) {
+          // activations are the consumers' own: nothing to load, no hand-off
+        } else if (i >= pre_s) {
           load_x(st + W_BYTES, ukt, 0, &full[slot]);
         } else if (i == pre_s - 1) {
           // the stages so far went out without their activations: wait for the image, then
@@ -238,7 +249,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
           handoff_wait();
           int kj = (int)(s0 - (int64_t)rb_first * nk);
           for (int j = 0; j < pre_s; ++j) {
-            load_x(tc::smem_u32(smem + (size_t)j * STAGE) + W_BYTES, kj, 0, &full[j]);
+            load_x(tc::smem_u32(smem + (size_t)j * STB) + W_BYTES, kj, 0, &full[j]);
             if (++kj == nk) kj = 0;
           }
           handoff_count();
@@ -278,21 +289,23 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
         ok = false;
         break;
       }
-      const uint32_t st = tc::smem_u32(smem + (size_t)slot * STAGE);
+      const uint32_t st = tc::smem_u32(smem + (size_t)slot * STB);
       const int xrow = KIND == S2_MOE_DN ? u * a.slot_rows : 0;  // first image row of this unit
       if (lane == 0) {
         // weights: chunks 2kt, 2kt+1 of rows rbl*128.. of expert ex -> smem [chunk][row][128 B]
         if (whole_chunks || (kt + 1) * S2_WB <= a.wbytes) {
-          tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + X_BYTES);
+          tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + XB);
           tma_load_4d_hint(st, &tmW, 0, rbl * S2_ROWS, kt * S2_CHUNKS, ex, &full[slot], wpol);
         } else {
           // the row ends inside this unit, off a chunk boundary: a chunk at a time from the 2D
           // view, whose bytes past the end (a whole chunk, possibly) are filled with zeros
-          tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + X_BYTES);
-          tc::tma_load_2d(smem + (size_t)slot * STAGE, &tmW2, kt * S2_WB, rbl * S2_ROWS, &full[slot]);
-          tc::tma_load_2d(smem + (size_t)slot * STAGE + W_CHUNK, &tmW2, kt * S2_WB + 128, rbl * S2_ROWS, &full[slot]);
+          tc::mbar_arrive_expect_tx(&full[slot], W_BYTES + XB);
+          tc::tma_load_2d(smem + (size_t)slot * STB, &tmW2, kt * S2_WB, rbl * S2_ROWS, &full[slot]);
+          tc::tma_load_2d(smem + (size_t)slot * STB + W_CHUNK, &tmW2, kt * S2_WB + 128, rbl * S2_ROWS, &full[slot]);
         }
-        if (i >= pre) {
+        if (loc) {
+          // activations are the consumers' own: nothing to load, no hand-off
+        } else if (i >= pre) {
           load_x(st + W_BYTES, kt, xrow, &full[slot]);
         } else if (i == pre - 1) {
           // the activation image is written by this grid's consumer warps: wait for it, then
@@ -305,7 +318,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
           int ktj = (int)(s0 - (int64_t)rb_first * nk), rbj = rb_first;
           for (int j = 0; j < pre; ++j) {  // pre <= S: stage j is slot j
             const int uj = kMoE ? rbj / a.nb : 0;
-            const uint32_t stj = tc::smem_u32(smem + (size_t)j * STAGE);
+            const uint32_t stj = tc::smem_u32(smem + (size_t)j * STB);
             load_x(stj + W_BYTES, ktj, KIND == S2_MOE_DN ? uj * a.slot_rows : 0, &full[j]);
             if (++ktj == nk) {
               ktj = 0;
@@ -317,7 +330,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
       }
       if constexpr (FMT == FMT_MXFP4) {
         // per-32 scale bytes of the unit: 128 rows x (8 bytes per chunk); bytes past K read as 0
-        const uint32_t sc = st + W_BYTES + X_BYTES;
+        const uint32_t sc = st + W_BYTES + XB;
         const uint8_t* sbase = a.wsb + (int64_t)ex * a.s_estride;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -355,13 +368,36 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
   // activations may come from the previous kernel in the stream: wait for it, then write this
   // CTA's jobs of the activation image (gate_up wrote them before routing)
   pdl_wait();
-  if constexpr (KIND != S2_MOE_GU) run_jobs(njob_rows, nsl);
+  const int kt0c = (int)(s0 - (int64_t)rb_first * nk);  // K unit of this CTA's first unit
+  if constexpr (kLocal)
+    s2_local_image<FMT>(a, tc::smem_u32(limg), kt0c, (int)min(s1 - s0, (int64_t)nk), threadIdx.x, s_red, s_tokf);
+  else if constexpr (KIND != S2_MOE_GU)
+    run_jobs(njob_rows, nsl);
   const int g = lane >> 2, t = lane & 3;
   const int gx = s2_rho(g);  // the activation row this thread's MMA column reads
   const int w = warp;  // 16-row tile of the unit
   // ldmatrix addressing: lane L feeds row 16w + (L & 7) + 8*((L >> 3) & 1) of piece 2p + (L >> 4)
   const int lrow = 16 * w + (lane & 7) + ((lane >> 3) & 1) * 8;
   const int lpc = lane >> 4;
+  // activation tiles: the stage's (TMA-loaded) or, with local activations, slot kt - kt0 of the
+  // CTA's own image, whose slabs hold only the M real rows (a thread's row is clamped to M - 1:
+  // the columns of padding tokens are never stored)
+  const uint32_t xsl = kLocal ? (uint32_t)(a.M * 128) : X_BOX;  // bytes between 64-K slabs
+  const uint32_t lslot = (uint32_t)(Tr::NXB * a.M * 128);
+  const uint32_t limg_s = tc::smem_u32(limg);
+  int xr_[MT];
+#pragma unroll
+  for (int m = 0; m < MT; ++m) xr_[m] = kLocal ? min(gx + 8 * m, a.M - 1) : gx + 8 * m;
+  auto xtile = [&](uint32_t st, int ktu) -> uint32_t {
+    if constexpr (!kLocal) {
+      return st + W_BYTES;
+    } else {
+      int sl = ktu - kt0c;
+      if (sl < 0) sl += nk;
+      return limg_s + (uint32_t)sl * lslot;
+    }
+  };
+  const float* tokf_p = kLocal ? s_tokf : a.tokf;  // the tokens' factors (x_s or 2^p)
 
   if (kCellCode && kDyn) {
     // INT8 units as the producer hands them over (slot -> row block, K unit).  A run of
@@ -369,8 +405,9 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
     // ends its sums go out as one atomic add per output cell (s2_cell_add), whose result is
     // inspected at the end of the next run, so the round trip overlaps that run's work: the add
     // that completed a cell's unit count settles the output, y = bf16((acc * x_s) * w_s) (+ bias
-    // after the cast).  The activation jobs zeroed the cells before the hand-off, and no stage
-    // reaches a consumer before it, so every cell starts the call at zero.
+    // after the cast).  Every cell starts the call at zero: left so by the previous call (the
+    // cell is reset once it has settled) or zeroed by the activation jobs before the hand-off,
+    // which no stage reaches a consumer before.
     int32_t acci[MT][4];
     unsigned long long pend[MT][4];  // cell values after this warp's last adds
     int pend_rb = -1;                // their row block (-1: none outstanding)
@@ -391,7 +428,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int col = s2_rho(2 * t + e2) + 8 * m;
-          xs[m][e2] = col < a.M ? a.tokf[col] : 0.f;
+          xs[m][e2] = col < a.M ? tokf_p[col] : 0.f;
         }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -407,6 +444,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
           const int row = pend_rb * S2_ROWS + row_g + (r >= 2 ? 8 : 0);
           if (row >= a.N || col >= a.M || s2_cell_units(pend[m][r]) != nk) continue;
           const int32_t v = s2_cell_sum(pend[m][r]);
+          if (a.cells_clean) a.cells[(int64_t)col * a.N + row] = 0ull;  // every add has arrived
           if (a.acc_out) a.acc_out[(int64_t)col * a.N + row] = v;
           if (!a.y) continue;  // a K shard: the int32 sums are the result
           uint16_t yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)v, xs[m][r & 1]), wsr[r >> 1]));
@@ -450,8 +488,8 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
       if (run > 0 && (urb != cur_rb || ukt != last_kt + 1)) post();
       cur_rb = urb;
       last_kt = ukt;
-      const uint32_t st = tc::smem_u32(smem + (size_t)slot * STAGE);
-      const uint32_t xt = st + W_BYTES;
+      const uint32_t st = tc::smem_u32(smem + (size_t)slot * STB);
+      const uint32_t xt = xtile(st, ukt);
       float ui[2][MT][4];  // two fp32 chains: integers below 2^24, exact
 #pragma unroll
       for (int e = 0; e < 2; ++e)
@@ -473,7 +511,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
           const int kx = 16 * pc + 4 * t;
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
-            const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(gx + 8 * m, (kx & 63) * 2));
+            const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * xsl + sw128(xr_[m], (kx & 63) * 2));
             mma_f16_16816(ui[pc & 1][m], a0, a1, a2, a3, xv.x, xv.y);
           }
         }
@@ -513,10 +551,10 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int col = s2_rho(2 * t + e2) + 8 * m;  // the token of MMA column 2t + e2
-        colf[m][e2] = col < cnt ? (kBF16 ? 1.f : a.tokf[(KIND == S2_MOE_DN ? eu * a.slot_rows : 0) + col]) : 0.f;
+        colf[m][e2] = col < cnt ? (kBF16 ? 1.f : tokf_p[(KIND == S2_MOE_DN ? eu * a.slot_rows : 0) + col]) : 0.f;
       }
     float rowf[2] = {1.f, 1.f}, rowb[2] = {0.f, 0.f};
-    if constexpr (KIND == S2_DENSE) {
+    if constexpr (!kMoE) {
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int row = min(row_w + g + 8 * e2, a.N - 1);
@@ -601,8 +639,8 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
         }
         continue;
       }
-      const uint32_t st = tc::smem_u32(smem + (size_t)slot * STAGE);
-      const uint32_t xt = st + W_BYTES;
+      const uint32_t st = tc::smem_u32(smem + (size_t)slot * STB);
+      const uint32_t xt = xtile(st, kt);
       // INT8 and per-channel FP8: the unit's sums in two fp32 chains.  For INT8 every partial sum
       // is an integer of at most 256 x 127 x 127 < 2^24 in magnitude, so they are exact and
       // convert once per unit
@@ -627,14 +665,14 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
           for (int p = 0; p < 4; ++p)
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-              const uint32_t xs = xt + ck * X_BOX;
-              const uint32_t b0 = lds32(xs + sw128(gx + 8 * m, 32 * p + 4 * t));
-              const uint32_t b1 = lds32(xs + sw128(gx + 8 * m, 32 * p + 16 + 4 * t));
+              const uint32_t xs = xt + ck * xsl;
+              const uint32_t b0 = lds32(xs + sw128(xr_[m], 32 * p + 4 * t));
+              const uint32_t b1 = lds32(xs + sw128(xr_[m], 32 * p + 16 + 4 * t));
               mma_bf16_16816(acc[m], q[p][0], q[p][1], q[p][2], q[p][3], b0, b1);
             }
         } else if constexpr (FMT == FMT_MXFP4) {
           // scale bytes of rows g and g+8 for the chunk's 8 groups
-          const uint32_t sbase = st + W_BYTES + X_BYTES;
+          const uint32_t sbase = st + W_BYTES + XB;
           const uint2 sa8 = lds64(sbase + (16 * w + g) * 16 + ck * 8);
           const uint2 sb8 = lds64(sbase + (16 * w + g + 8) * 16 + ck * 8);
 #pragma unroll
@@ -646,7 +684,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
             uint4 xv[MT];
 #pragma unroll
             for (int m = 0; m < MT; ++m)
-              xv[m] = lds128(xt + (4 * ck + (kx >> 6)) * X_BOX + sw128(gx + 8 * m, (kx & 63) * 2));
+              xv[m] = lds128(xt + (4 * ck + (kx >> 6)) * xsl + sw128(xr_[m], (kx & 63) * 2));
             float blk[MT][4];
 #pragma unroll
             for (int m = 0; m < MT; ++m) blk[m][0] = blk[m][1] = blk[m][2] = blk[m][3] = 0.f;
@@ -690,7 +728,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
             const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-              const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(gx + 8 * m, (kx & 63) * 2));
+              const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * xsl + sw128(xr_[m], (kx & 63) * 2));
               mma_f16_16816(ui[pc & 1][m], a0, a1, a2, a3, xv.x, xv.y);
             }
           }
@@ -704,7 +742,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
             const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-              const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(gx + 8 * m, (kx & 63) * 2));
+              const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * xsl + sw128(xr_[m], (kx & 63) * 2));
               mma_f16_16816(ui[pc & 1][m], a0, a1, a2, a3, xv.x, xv.y);
             }
           }
@@ -726,7 +764,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
               const int kx = 16 * pc + 4 * t;  // K within the chunk of this thread's 4 weights
 #pragma unroll
               for (int m = 0; m < MT; ++m) {
-                const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * X_BOX + sw128(gx + 8 * m, (kx & 63) * 2));
+                const uint2 xv = lds64(xt + (2 * ck + (kx >> 6)) * xsl + sw128(xr_[m], (kx & 63) * 2));
                 mma_f16_16816(blk[j & 1][m], a0, a1, a2, a3, xv.x, xv.y);
               }
             }
@@ -787,7 +825,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
     }
     // another CTA settles it: store the partial sums in this CTA's slot (a CTA posts at most
     // once: for its first segment), then count in with release order
-    float* pb = a.part + (int64_t)c * 16 * S2_ROWS;
+    float* pb = a.part + (int64_t)c * Mp * S2_ROWS;
 #pragma unroll
     for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -841,7 +879,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
           const int rl = 16 * w + g + (r >= 2 ? 8 : 0);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            v[m][r][k] = (u0 + k < count) ? __ldcg(a.part + ((int64_t)(c + u0 + k) * 16 + col) * S2_ROWS + rl) : 0.f;
+            v[m][r][k] = (u0 + k < count) ? __ldcg(a.part + ((int64_t)(c + u0 + k) * Mp + col) * S2_ROWS + rl) : 0.f;
         }
 #pragma unroll
       for (int m = 0; m < MT; ++m)

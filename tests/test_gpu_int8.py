@@ -23,8 +23,8 @@ def run(ql, c, bias=None, wsl=None):
     b = None if bias is None else to_bf16_tensor(bias)
     y, acc, xq, xs, path = ql.qlinear_int8_w8a8(x, w, ws, b, debug=True)
     torch.cuda.synchronize()
-    # up to 16 tokens: the persistent skinny kernel; more: the tcgen05 GEMM
-    assert path == ("int8_skinny" if c["x"].shape[0] <= 16 else "int8_tcgen05")
+    # up to 32 tokens: the persistent skinny kernel; more: the tcgen05 GEMM
+    assert path == ("int8_skinny" if c["x"].shape[0] <= 32 else "int8_tcgen05")
     return bits_of(y), acc.cpu().numpy(), xq.cpu().numpy(), xs.cpu().numpy()
 
 
@@ -83,8 +83,15 @@ def test_int8_full_size_sampled(ql, N, K, M):
     compare(c, run(ql, c), rows=rows)
 
 
+@pytest.mark.parametrize("M,N,K", [(17, 300, 2048), (24, 1000, 4096), (32, 130, 17408), (31, 4097, 640)])
+def test_int8_skinny_up_to_32_tokens(ql, M, N, K):
+    # 17..32 tokens: the persistent kernel with four 8-token MMA tiles
+    c = synth.int8_case(M, N, K, seed=M * 3 + N)
+    compare(c, run(ql, c))
+
+
 @pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408), (10240, 5120)])
-@pytest.mark.parametrize("M", [4, 16])
+@pytest.mark.parametrize("M", [4, 16, 32])
 def test_int8_full_size_every_row(ql, N, K, M):
     # every output row against the oracle: units are claimed at run time, so any row block
     # may be split between CTAs in a different way on each call
@@ -157,7 +164,7 @@ def test_int8_gemm_zero_token_and_large_values(ql):
 
 
 @pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408), (10240, 5120)])
-@pytest.mark.parametrize("M", [32, 256])
+@pytest.mark.parametrize("M", [32, 64, 256])
 def test_int8_gemm_full_size_sampled(ql, N, K, M):
     c = synth.int8_case(M, N, K, seed=1)
     rows = sample_rows(N, seed=M)

@@ -19,7 +19,8 @@ def ql():
 
 
 # ------------------------------------------------------------------ MXFP4 dense, bf16 activations
-@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (7, 130, 1024), (16, 512, 4096), (3, 64, 96)])
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (7, 130, 1024), (16, 512, 4096), (3, 64, 96), (2, 2048, 8192),
+                                   (1, 1000, 40960)])
 def test_mxfp4_dense_bf16(ql, M, N, K):
     c = synth.mxfp4_dense_case(M, N, K, seed=M + N)
     x = to_bf16_tensor(c["x"])

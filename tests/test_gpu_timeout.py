@@ -23,7 +23,9 @@ def ql():
 
 
 def test_wait_timeout_is_reported_and_recoverable(ql):
-    c = synth.int8_case(2, 640, 2048, seed=7)
+    # M * K above the local-activation limit: the call shares one activation image, so its
+    # producers wait for the image at the hand-off
+    c = synth.int8_case(3, 640, 16384, seed=7)
     x = to_bf16_tensor(c["x"])
     w = torch.from_numpy(c["w"]).cuda()
     s = torch.from_numpy(c["w_s"]).cuda()
@@ -59,3 +61,89 @@ def test_wait_timeout_is_reported_and_recoverable(ql):
     assert np.array_equal(call(), ref["acc"])
     st, flags = ql.read_device_status(ws.buf)
     assert st == 0 and flags == 0
+
+
+def _timeout_then_exact(ql, call, check):
+    """Run `call` (returns host results) with the wait limit at 0 until the status word shows
+    QL_DEV_TIMEOUT, then with the default limit on a re-initialised workspace: `check` must
+    pass again.  `call(ws)` takes the workspace to use."""
+    ws = ql.Workspace()
+    check(call(ws))
+    st, flags = ql.read_device_status(ws.buf)
+    assert st == 0 and flags == 0
+    ql.set_wait_limit(0)
+    try:
+        seen = False
+        for _ in range(8):
+            call(ws)
+            st, flags = ql.read_device_status(ws.buf, clear=True)
+            if flags & DEV_TIMEOUT:
+                seen = True
+                break
+    finally:
+        ql.set_wait_limit(DEFAULT_WAIT_LIMIT)
+    assert seen and st != 0, "a zero wait limit never timed out"
+    ws.buf.zero_()
+    torch.cuda.synchronize()
+    check(call(ws))
+    st, flags = ql.read_device_status(ws.buf)
+    assert st == 0 and flags == 0
+
+
+def test_int8_tcgen05_gemm_timeout_is_reported_and_recoverable(ql):
+    """M > 16: the tcgen05 INT8 GEMM (producer, widening warps, MMA issuer and drain warps all
+    bound their waits; in-flight loads and MMAs are waited for and tensor memory is freed)."""
+    c = synth.int8_case(40, 384, 2048, seed=8)
+    x, w, s = to_bf16_tensor(c["x"]), torch.from_numpy(c["w"]).cuda(), torch.from_numpy(c["w_s"]).cuda()
+    ref = Q.int8_w8a8(c["x"], c["w"], c["w_s"])
+
+    def call(ws):
+        _, acc, _, _, path = ql.qlinear_int8_w8a8(x, w, s, debug=True, workspace=ws)
+        torch.cuda.synchronize()
+        assert path == "int8_tcgen05"
+        return acc.cpu().numpy()
+
+    _timeout_then_exact(ql, call, lambda acc: np.testing.assert_array_equal(acc, ref["acc"]))
+
+
+def test_block_scaled_tcgen05_gemm_timeout_is_reported_and_recoverable(ql):
+    """The block-scaled tcgen05 GEMM (FP8 weights, 1x128 E4M3 activations)."""
+    from oracle import formats as F
+    from _util import bits_of, check_float
+    c = synth.fp8_block_case(64, 256, 1024, seed=9)
+    x, w, s = to_bf16_tensor(c["x"]), torch.from_numpy(c["w"]).cuda(), torch.from_numpy(c["s"]).cuda()
+    ref = Q.fp8_block_act_quant(c["x"], c["w"], c["s"], 1024)
+
+    def call(ws):
+        y, _, _, path = ql.qlinear_fp8_block(x, w, s, act_mode=ql.ACT_E4M3_1X128, debug=True, workspace=ws)
+        torch.cuda.synchronize()
+        assert path == "fp8_tcgen05"
+        return bits_of(y)
+
+    _timeout_then_exact(ql, call, lambda y: check_float(y, ref["y_f64"], ref["abs_sum"]))
+
+
+def test_grouped_moe_timeout_is_reported_and_recoverable(ql):
+    """M > 16 MoE: routing, dispatch and the two grouped tcgen05 GEMMs."""
+    c = synth.moe_case(20, E=8, H=256, I=256, seed=10)
+    wd = [torch.from_numpy(c[k]).cuda() for k in ("w13", "s13", "w2", "s2")]
+    x, lg = to_bf16_tensor(c["x"]), to_bf16_tensor(c["logits"])
+    rid, _ = Q.route_topk(c["logits"], 2)
+
+    def call(ws):
+        y, ids, _, _, path = ql.moe_mxfp4_grouped(x, *wd, router_logits=lg, topk=2, debug=True, workspace=ws)
+        torch.cuda.synchronize()
+        assert path == "moe_mxfp4_tcgen05"
+        return ids.cpu().numpy(), y.float().cpu().numpy()
+
+    first = {}
+
+    def check(res):
+        ids, y = res
+        np.testing.assert_array_equal(ids, rid)
+        if "y" in first:  # the same inputs give the same outputs once the workspace is clean
+            np.testing.assert_array_equal(y, first["y"])
+        else:
+            first["y"] = y
+
+    _timeout_then_exact(ql, call, check)
