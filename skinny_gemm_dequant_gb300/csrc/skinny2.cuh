@@ -293,6 +293,7 @@ __device__ __forceinline__ void s2_conv8(const uint4 u, float f, float inv, bool
 template <int FMT>
 __device__ void s2_prepare(const Skinny2Args& a, int m, int sl, int nsl, int tid, float* red) {
   constexpr int V = 8;  // 16-byte vectors a thread holds: one pass over x for K <= 256*8*8
+  constexpr bool kCompact = FMT != FMT_MXFP4;
   const uint16_t* xr = a.x + (int64_t)m * a.ldx;
   const int nvec = a.K / 8;
   const int v0 = (int)((int64_t)sl * nvec / nsl), v1 = (int)((int64_t)(sl + 1) * nvec / nsl);
@@ -300,10 +301,16 @@ __device__ void s2_prepare(const Skinny2Args& a, int m, int sl, int nsl, int tid
   uint4 v[V];
   float amax = 0.f;
   if (one_pass) {
+    // thread tid holds vectors v0 + tid + 256 j (wrapping at the row end): the whole row for the
+    // amax, and first the one of the slice it converts, so the conversion below is one copy of
+    // its code (this code runs once per call, from a cold instruction cache)
+    // (MXFP4 keeps the plain order: its MoE kernels run at the register cap of two CTAs per SM)
 #pragma unroll
     for (int j = 0; j < V; ++j) {
-      const int i = tid + 256 * j;
-      v[j] = i < nvec ? *reinterpret_cast<const uint4*>(xr + 8 * i) : make_uint4(0, 0, 0, 0);
+      const int t = tid + 256 * j;
+      int i = kCompact ? v0 + t : t;
+      if (kCompact && i >= nvec) i -= nvec;
+      v[j] = t < nvec ? *reinterpret_cast<const uint4*>(xr + 8 * i) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int j = 0; j < V; ++j)
@@ -332,7 +339,11 @@ __device__ void s2_prepare(const Skinny2Args& a, int m, int sl, int nsl, int tid
     const uint4 hv = make_uint4(h[0], h[1], h[2], h[3]);
     for (int cp = 0; cp < a.xcopies; ++cp) *reinterpret_cast<uint4*>(out + cp * cstride + 8 * i) = hv;
   };
-  if (one_pass) {
+  if (one_pass && kCompact) {
+    if (tid < v1 - v0) conv(v[0], v0 + tid);
+    for (int t = tid + 256; t < v1 - v0; t += 256)  // slices above 256 vectors
+      conv(*reinterpret_cast<const uint4*>(xr + 8 * (v0 + t)), v0 + t);
+  } else if (one_pass) {
 #pragma unroll
     for (int j = 0; j < V; ++j) {
       const int i = tid + 256 * j;
