@@ -295,6 +295,7 @@ def build_c3(ql, torch, limit=None, name="c3", Ms=None):
         b = uniq * bytes_moe_expert(H, I) + 2 * M * H * 2 + 2 * M * E
         calls.append({"fn": call, "M": M, "N": H, "K": I, "bytes": b, "flops": 2 * M * topk * 3 * H * I,
                       "x": sets[0][0], "y": y, "kind": "moe_tcgen05" if grouped else "moe",
+                      "inputs": [t for st in sets for t in st[:2]],  # every rotation's x and logits
                       "unique_experts": uniq})
     cfg = {"workload": WORKLOADS[name],
            "bytes": "unique touched experts x 13369344 B + x + logits + y"}
@@ -495,19 +496,36 @@ def time_per_call(wl, torch, uses=32, reps=8):
     return out
 
 
+def rehome(torch, tensors):
+    """Re-point bf16 device tensors, in place (Tensor.set_), at consecutive 128-byte aligned views
+    of one device buffer, which is returned: the calls keep using the same tensor objects, and a
+    single copy then moves all of them."""
+    uniq = list({id(t): t for t in tensors}.values())
+    sizes = [-(-t.numel() // 64) * 64 for t in uniq]
+    arena = torch.zeros(sum(sizes), dtype=torch.bfloat16, device="cuda")
+    off = 0
+    for t, n in zip(uniq, sizes):
+        assert t.dtype == torch.bfloat16 and t.is_contiguous()
+        arena[off:off + t.numel()].copy_(t.reshape(-1))
+        t.set_(arena.untyped_storage(), off, t.size(), t.stride())
+        off += n
+    return arena
+
+
 def time_e2e(wl, steps, torch):
-    """Through the public API with host buffers: each call copies its activations from pinned
-    host memory, runs, and copies its output back to pinned host memory, all inside the timed
-    region (the step's calls and copies captured in CUDA graphs, replayed)."""
+    """Through the public API with host buffers: every step copies all of its activations from
+    pinned host memory in one copy, runs its calls, and copies all of its outputs back to pinned
+    host memory in one copy, inside the timed region (captured in CUDA graphs, replayed).  The
+    activations and outputs of the step's calls live in one device buffer each (rehome)."""
     st = torch.cuda.current_stream()
-    hx = [c["x"].cpu().pin_memory() for c in wl.calls]
-    hy = [torch.empty(c["y"].shape, dtype=c["y"].dtype).pin_memory() for c in wl.calls]
+    hx = wl.x_arena.cpu().pin_memory()
+    hy = torch.empty(wl.y_arena.shape, dtype=wl.y_arena.dtype).pin_memory()
 
     def body():
-        for i, c in enumerate(wl.calls):
-            c["x"].copy_(hx[i], non_blocking=True)
+        wl.x_arena.copy_(hx, non_blocking=True)
+        for c in wl.calls:
             c["fn"]()
-            hy[i].copy_(c["y"], non_blocking=True)
+        hy.copy_(wl.y_arena, non_blocking=True)
     graphs = [capture(torch, body) for _ in range(ROTATE)]
     for g in graphs:
         g.replay()
@@ -518,9 +536,7 @@ def time_e2e(wl, steps, torch):
         graphs[i % len(graphs)].replay()
     b.record(st)
     b.synchronize()
-    h2d = sum(t.numel() * t.element_size() for t in hx)
-    d2h = sum(t.numel() * t.element_size() for t in hy)
-    return a.elapsed_time(b), h2d, d2h
+    return a.elapsed_time(b), hx.numel() * hx.element_size(), hy.numel() * hy.element_size()
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -743,6 +759,9 @@ def main():
         pg = dist
     import skinny_gemm_dequant_gb300 as ql
     wl = BUILDERS[args.config](ql, torch)
+    # the step's activations and outputs in one device buffer each (one copy per step end to end)
+    wl.x_arena = rehome(torch, [t for c in wl.calls for t in c.get("inputs", [c["x"]])])
+    wl.y_arena = rehome(torch, [c["y"] for c in wl.calls])
     for c in wl.calls:  # sizes the shared workspace before any capture
         c["fn"]()
     torch.cuda.synchronize()
