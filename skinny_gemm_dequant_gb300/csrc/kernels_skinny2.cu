@@ -102,6 +102,7 @@ static cudaError_t launch2(const Skinny2Plan& p, Skinny2Args a, const uint8_t* w
   uint32_t stage_bytes = STAGE;
   if (KIND == S2_DENSE_LOCAL) {
     const int64_t slots = p.units_per_cta < p.nk ? p.units_per_cta : p.nk;
+    if (slots * (Tr::KPU / 8) > 1024) return cudaErrorNotSupported;  // s2_local_image holds <= 4 vectors a thread
     const size_t lb = ((size_t)slots * Tr::NXB * a.M * 128 + 127) & ~size_t(127);
     const uint32_t sb = S2_ROWS * S2_WB + Tr::SCB;
     int SL = (optin > (int)(fixed + lb)) ? (int)((optin - fixed - lb) / (sb + 16)) : 0;

@@ -380,13 +380,25 @@ template <int FMT>
 __device__ void s2_local_image(const Skinny2Args& a, uint32_t L, int kt0, int n_slots, int tid, float* red,
                                float* tokf) {
   constexpr int KPU = S2Traits<FMT>::KPU, VPU = KPU / 8;  // 8-element vectors per unit
+  constexpr int KEEP = 4;  // vectors of the CTA's own units a thread holds (the host keeps n_slots * VPU <= 1024)
   const int nvec = a.K / 8, M = a.M;
+  const int nneed = n_slots * VPU;
   const uint32_t slot_bytes = (uint32_t)(S2Traits<FMT>::NXB * M * 128);
-  __shared__ float s_inv[16];
-  __shared__ int s_fast[16];
   for (int m = 0; m < M; ++m) {
     const uint16_t* xr = a.x + (int64_t)m * a.ldx;
+    // the vectors of this CTA's units (thread tid: t = tid + 256 j) and, at the same time, the
+    // whole row for the amax: every load goes out before any result is used (one round trip)
+    uint4 keep[KEEP];
+#pragma unroll
+    for (int j = 0; j < KEEP; ++j) {
+      const int t = tid + 256 * j;
+      int kt = kt0 + t / VPU;
+      if (kt >= a.nk) kt -= a.nk;
+      const int vi = kt * VPU + t % VPU;
+      keep[j] = (t < nneed && vi < nvec) ? *reinterpret_cast<const uint4*>(xr + 8 * vi) : make_uint4(0, 0, 0, 0);
+    }
     float amax = 0.f;
+#pragma unroll 4
     for (int i = tid; i < nvec; i += 256) {
       const uint4 u = *reinterpret_cast<const uint4*>(xr + 8 * i);
       amax = fmaxf(amax, fmaxf(fmaxf(bf16x2_absmax(u.x), bf16x2_absmax(u.y)), fmaxf(bf16x2_absmax(u.z), bf16x2_absmax(u.w))));
@@ -394,37 +406,40 @@ __device__ void s2_local_image(const Skinny2Args& a, uint32_t L, int kt0, int n_
     amax = warp_max(amax);
     if ((tid & 31) == 0) red[tid >> 5] = amax;
     consumer_sync();
+    amax = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])), fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7])));
+    if (FMT == FMT_INT8 && a.amax_in) amax = a.amax_in[m];  // a K shard: the whole row's amax
+    float f, inv;
+    bool fast;
+    s2_token_factors<FMT>(amax, f, inv, fast);
     if (tid == 0) {
-      amax = fmaxf(fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])), fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7])));
-      if (FMT == FMT_INT8 && a.amax_in) amax = a.amax_in[m];  // a K shard: the whole row's amax
-      float f, inv;
-      bool fast;
-      s2_token_factors<FMT>(amax, f, inv, fast);
       tokf[m] = f;
-      s_inv[m] = inv;
-      s_fast[m] = fast;
       if (FMT == FMT_INT8 && a.xs_dbg && blockIdx.x == 0) a.xs_dbg[m] = f;
+    }
+    // one copy of the conversion code (it runs once per call, from a cold instruction cache):
+    // the held vectors are picked by selects, not by unrolling the loop
+#pragma unroll 1
+    for (int j = 0; j < KEEP; ++j) {
+      const int t = tid + 256 * j;
+      if (t >= nneed) break;
+      uint4 u = keep[0];
+#pragma unroll
+      for (int q = 1; q < KEEP; ++q)
+        if (j == q) u = keep[q];
+      const int sl = t / VPU, c8 = t - sl * VPU;
+      int kt = kt0 + sl;
+      if (kt >= a.nk) kt -= a.nk;
+      const int k = kt * KPU + c8 * 8;
+      uint32_t h[4], qb[2];
+      s2_conv8<FMT>(u, f, inv, fast, h, qb);
+      if (FMT == FMT_INT8 && a.xq_dbg && k < a.K)
+        *reinterpret_cast<uint2*>(a.xq_dbg + (int64_t)m * a.K + k) = make_uint2(qb[0], qb[1]);
+      const int jj = c8 >> 3, c16 = c8 & 7;  // slab, 16-byte chunk of the 128-byte row
+      const uint32_t dst = L + (uint32_t)sl * slot_bytes + (uint32_t)(jj * M + m) * 128u + (uint32_t)((c16 ^ (m & 7)) << 4);
+      asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                   : "memory");
     }
     consumer_sync();  // red[] is reused by the next token
   }
-  const int total = n_slots * VPU * M;
-  for (int v = tid; v < total; v += 256) {
-    const int m = v % M, rest = v / M;
-    const int sl = rest / VPU, c8 = rest - sl * VPU;
-    int kt = kt0 + sl;
-    if (kt >= a.nk) kt -= a.nk;
-    const int k = kt * KPU + c8 * 8;
-    const uint4 u = k < a.K ? *reinterpret_cast<const uint4*>(a.x + (int64_t)m * a.ldx + k) : make_uint4(0, 0, 0, 0);
-    uint32_t h[4], qb[2];
-    s2_conv8<FMT>(u, tokf[m], s_inv[m], s_fast[m] != 0, h, qb);
-    if (FMT == FMT_INT8 && a.xq_dbg && k < a.K)
-      *reinterpret_cast<uint2*>(a.xq_dbg + (int64_t)m * a.K + k) = make_uint2(qb[0], qb[1]);
-    const int j = c8 >> 3, c16 = c8 & 7;  // slab, 16-byte chunk of the 128-byte row
-    const uint32_t dst = L + (uint32_t)sl * slot_bytes + (uint32_t)(j * M + m) * 128u + (uint32_t)((c16 ^ (m & 7)) << 4);
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
-                 : "memory");
-  }
-  consumer_sync();
 }
 
 // MoE down activations, one job = (dispatch position q, slice sl of nsl).  The pair p = m*topk+j
