@@ -433,17 +433,16 @@ BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4"
             "n4": build_n4}
 
 _SKINNY = ("skinny2_kernel (one launch per call: activation preparation + weight-streaming GEMM); "
-           "achieved = algorithmic bytes per call / CUDA-event time per call (graphs of 32 back-to-back "
-           "calls), aggregated over the step's calls")
-_MOE = ("MoE launches per call (gate_up with the routing fused in, down, combine); bytes of the touched "
-        "experts / event time per call")
+           "achieved = the step's algorithmic bytes / the step's device time")
+_MOE = ("MoE launches per call (gate_up with the routing fused in, down, combine); the step's touched-expert "
+        "bytes / the step's device time")
 KERNEL_DESC = {"c0": _SKINNY, "c1": _SKINNY, "c2": _SKINNY, "n2": _SKINNY, "n4": _SKINNY,
                "c3": _MOE, "n3": _MOE,
                "n5": "grouped MoE launches per call (routing, dispatch, activation quantisation, two grouped "
-                     "tcgen05 GEMMs, h quantisation, combine); bytes of the touched experts / event time per call",
-               "c4": "tcgen05 block-scaled GEMM + its activation-quantisation launch; bytes / event time per call",
-               "n1": "INT8 for M > 16: skinny2_kernel (M = 32) or the tcgen05 GEMM + its per-token quantisation "
-                     "launch (M > 32); bytes / event time per call"}
+                     "tcgen05 GEMMs, h quantisation, combine); the step's touched-expert bytes / device time",
+               "c4": "tcgen05 block-scaled GEMM + its activation-quantisation launch; the step's bytes / device time",
+               "n1": "INT8 for M = 32..256: skinny2_kernel (M = 32) or the tcgen05 GEMM + its per-token quantisation "
+                     "launch (M > 32); the step's bytes / device time"}
 
 
 # ----------------------------------------------------------------------------- timing

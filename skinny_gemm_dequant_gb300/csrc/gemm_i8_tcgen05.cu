@@ -198,10 +198,12 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       for (int kt = 0; kt < pre; ++kt)
         tma_load_2d(stage_ptr(kt) + kI8A8Bytes + kI8A16Bytes, &tmB, (kt0 + kt) * kI8BlockK, t0, &tma_full[kt]);
       int issued = pre;
+      // slot and phase kept incrementally: one thread runs this loop, so its instruction count
+      // per stage paces the ring (no divisions by the runtime stage count)
+      int s = pre == S ? 0 : pre;
+      uint32_t ph = 0;  // parity of the slot's previous use
       for (int kt = pre; kt < nk; ++kt) {
-        const int s = kt % S;
-        const uint32_t it = kt / S;
-        if (!mbar_wait(&empty[s], (it - 1) & 1, lim, abort)) {
+        if (!mbar_wait(&empty[s], ph, lim, abort)) {
           fail();
           break;
         }
@@ -209,6 +211,10 @@ __global__ void __launch_bounds__(kI8Threads, 1)
         tma_load_2d(stage_ptr(s), &tmA, (kt0 + kt) * kI8BlockK, n0, &tma_full[s]);
         tma_load_2d(stage_ptr(s) + kI8A8Bytes + kI8A16Bytes, &tmB, (kt0 + kt) * kI8BlockK, t0, &tma_full[s]);
         issued = kt + 1;
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
       if (*abort) {
         // no copy may land after the CTA exits: wait for the last load of every stage
@@ -224,9 +230,12 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       const uint64_t a_desc0 = smem_desc_sw128(smem_u32(smem + kI8A8Bytes));
       const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem + kI8A8Bytes + kI8A16Bytes));
       const uint32_t step = stage >> 4;
+      // slot, parity and descriptor offset kept incrementally: this thread's instructions per
+      // stage pace the tensor core (a division by the runtime stage count cost ~10 % of a call)
+      int s = 0;
+      uint32_t par = 0;
+      uint64_t doff = 0;
       for (int kt = 0; kt < nk; ++kt) {
-        const int s = kt % S;
-        const uint32_t par = (uint32_t)(kt / S) & 1;
         const int g = kt / kI8GroupStages;
         const bool first = kt % kI8GroupStages == 0;
         const uint32_t buf = tmem + (uint32_t)(g & 1) * 128u;
@@ -240,12 +249,18 @@ __global__ void __launch_bounds__(kI8Threads, 1)
           break;
         }
         tc_fence_after();
-        const uint64_t ad = a_desc0 + (uint64_t)((uint32_t)s * step), bd = b_desc0 + (uint64_t)((uint32_t)s * step);
+        const uint64_t ad = a_desc0 + doff, bd = b_desc0 + doff;
         // four 16-K steps (32 bytes = 2 descriptor units each)
 #pragma unroll
         for (int j = 0; j < 4; ++j) mma_f16(buf, ad + 2 * j, bd + 2 * j, idesc, (first && j == 0) ? 0u : 1u);
         tc_commit(&empty[s]);
         if (kt % kI8GroupStages == kI8GroupStages - 1 || kt == nk - 1) tc_commit(&acc_full[g & 1]);
+        doff += step;
+        if (++s == S) {
+          s = 0;
+          par ^= 1u;
+          doff = 0;
+        }
       }
       tc_commit(done);
       if (*abort) mbar_wait(done, 0, kI8DrainLimit, nullptr);
@@ -255,9 +270,9 @@ __global__ void __launch_bounds__(kI8Threads, 1)
     // each warp widens 32 rows per stage, 8 rows per pass: lane = (row within the pass, 16-byte
     // chunk); the f16 row is 128 bytes, chunk j of row r stored at chunk j ^ (r & 7)
     const int cw = warp - 4;
+    int s = 0;
+    uint32_t par = 0;
     for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % S;
-      const uint32_t par = (uint32_t)(kt / S) & 1;
       int got = 0;
       if (lane == 0) got = mbar_wait(&tma_full[s], par, lim, abort);
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -291,6 +306,10 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&conv_full[s]);
+      if (++s == S) {
+        s = 0;
+        par ^= 1u;
+      }
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ drain + epilogue

@@ -159,10 +159,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();  // activation codes come from the quantisation kernel
     for (int kt = 0; kt < pre; ++kt) tma_load_2d(sB + (size_t)kt * b_bytes, &tmB, kt * kBlockK, t0, &tma_full[kt]);
     int issued = pre;
+    // slot and phase kept incrementally (no divisions by the runtime stage count in a loop one
+    // thread runs per stage)
+    int s = pre == S ? 0 : pre;
+    uint32_t ph = 0;  // parity of the slot's previous use
     for (int kt = pre; kt < nk; ++kt) {
-      const int s = kt % S;
-      const uint32_t it = kt / S;
-      if (!mbar_wait(&empty[s], (it - 1) & 1, lim, abort)) {
+      if (!mbar_wait(&empty[s], ph, lim, abort)) {
         fail();
         break;
       }
@@ -170,6 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_a(sA + (size_t)s * a_bytes, kt, &tma_full[s]);
       tma_load_2d(sB + (size_t)s * b_bytes, &tmB, kt * kBlockK, t0, &tma_full[s]);
       issued = kt + 1;
+      if (++s == S) {
+        s = 0;
+        ph ^= 1u;
+      }
     }
     if (*abort) {
       // no copy may land after the CTA exits: wait for the last load of every stage
@@ -189,16 +195,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t a_step = a_bytes >> 4, b_step = b_bytes >> 4, b_sub = ((uint32_t)p.sub_n * kBlockK) >> 4;
     const uint32_t sf_stride = 4 + 4 * (uint32_t)p.nsub;
     const bool two = p.nsub > 1;
+    // slot, parity and the stage's descriptor / scale-column offsets kept incrementally: this
+    // thread's instructions per stage pace the tensor core
+    int s = 0;
+    uint32_t par = 0;
+    uint64_t aoff = 0, boff = 0;
+    uint32_t sfoff = 0;
     for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % S;
-      const uint32_t par = (uint32_t)(kt / S) & 1;
       if (!mbar_wait(&tma_full[s], par, lim, abort) || !mbar_wait(&sf_full[s], par, lim, abort)) {
         fail();
         break;
       }
       tc_fence_after();
-      const uint64_t ad = a_desc0 + (uint64_t)((uint32_t)s * a_step), bd = b_desc0 + (uint64_t)((uint32_t)s * b_step);
-      const uint32_t sfa = tmem + kSfCol0 + (uint32_t)s * sf_stride;
+      const uint64_t ad = a_desc0 + aoff, bd = b_desc0 + boff;
+      const uint32_t sfa = tmem + kSfCol0 + sfoff;
       // four 32-K steps (32 bytes = 2 descriptor units each), scale byte j of each vector
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -208,6 +218,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (kt > 0 || j > 0) ? 1u : 0u);
       }
       tc_commit(&empty[s]);
+      aoff += a_step;
+      boff += b_step;
+      sfoff += sf_stride;
+      if (++s == S) {
+        s = 0;
+        par ^= 1u;
+        aoff = boff = 0;
+        sfoff = 0;
+      }
     }
     tc_commit(acc_full);  // completes once every MMA issued above has finished
     if (*abort) mbar_wait(acc_full, 0, kDrainLimit, nullptr);
@@ -287,17 +306,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 #pragma unroll
     for (int d = 0; d < kPD; ++d) fetch(d, pw[d], pb[d]);
+    int s = 0;
+    uint32_t ph = 1;  // parity of the slot's previous use (a fresh barrier passes parity 1)
     for (int k0 = 0; k0 < nk && ok; k0 += kPD) {
 #pragma unroll
       for (int d = 0; d < kPD; ++d) {
         const int kt = k0 + d;
         if (kt >= nk) break;
-        const int s = kt % S;
-        const uint32_t it = kt / S;
         // lane 0 waits and the result is broadcast, so the warp stays converged for the
         // .sync.aligned tensor-memory stores below
         int got = 0;
-        if (lane == 0) got = mbar_wait(&empty[s], (it - 1) & 1, lim, abort);
+        if (lane == 0) got = mbar_wait(&empty[s], ph, lim, abort);
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
           if (lane == 0) fail();
@@ -316,6 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sf_full[s]);
         fetch(kt + kPD, pw[d], pb[d]);
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
       }
     }
     int got = 0;
