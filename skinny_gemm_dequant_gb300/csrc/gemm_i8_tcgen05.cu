@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       int s = 0;
       uint32_t par = 0;
       uint64_t doff = 0;
+      uint32_t ready = 0;  // bits 0 / 1: this stage's TMA / conversion barriers already seen complete
       for (int kt = 0; kt < nk; ++kt) {
         const int g = kt / kI8GroupStages;
         const bool first = kt % kI8GroupStages == 0;
@@ -244,15 +245,17 @@ __global__ void __launch_bounds__(kI8Threads, 1)
           fail();
           break;
         }
-        if (!mbar_wait(&tma_full[s], par, lim, abort) || !mbar_wait(&conv_full[s], par, lim, abort)) {
+        if ((!(ready & 1) && !mbar_wait(&tma_full[s], par, lim, abort)) ||
+            (!(ready & 2) && !mbar_wait(&conv_full[s], par, lim, abort))) {
           fail();
           break;
         }
         tc_fence_after();
         const uint64_t ad = a_desc0 + doff, bd = b_desc0 + doff;
-        // four 16-K steps (32 bytes = 2 descriptor units each)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) mma_f16(buf, ad + 2 * j, bd + 2 * j, idesc, (first && j == 0) ? 0u : 1u);
+        // the next stage's slot and parity, whose barriers are tested while these MMAs issue
+        const int sn = s + 1 == S ? 0 : s + 1;
+        const uint32_t pn = s + 1 == S ? par ^ 1u : par;
+        ready = mma4_f16_test2(buf, ad, bd, idesc, first ? 0u : 1u, smem_u32(&tma_full[sn]), smem_u32(&conv_full[sn]), pn);
         tc_commit(&empty[s]);
         if (kt % kI8GroupStages == kI8GroupStages - 1 || kt == nk - 1) tc_commit(&acc_full[g & 1]);
         doff += step;

@@ -120,6 +120,33 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       : "memory");
 }
 
+// One 64-K stage of f16 MMAs (four K = 16 steps: descriptors advance by 2 units = 32 bytes)
+// issued in the same instruction stream as a non-blocking test of the next stage's two
+// barriers: a completed-phase test costs ~150 cycles of latency in the issuing thread, which
+// the MMA issue (~110 cycles each) hides.  Returns bit 0 / bit 1 = barrier 0 / 1 complete.
+__device__ __forceinline__ uint32_t mma4_f16_test2(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate, uint32_t bar0, uint32_t bar1,
+                                                   uint32_t parity) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p0, p1, pa;\n\t.reg .u32 r0, r1;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p0, [%6], %8;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p1, [%7], %8;\n\t"
+      "setp.ne.b32 pa, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, pa;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %9, %10, %4, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %11, %12, %4, 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%1], %13, %14, %4, 1;\n\t"
+      "selp.u32 r0, 1, 0, p0;\n\t"
+      "selp.u32 r1, 2, 0, p1;\n\t"
+      "or.b32 %0, r0, r1;\n\t}"
+      : "=r"(r)
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(bar0), "r"(bar1), "r"(parity),
+        "l"(a_desc + 2), "l"(b_desc + 2), "l"(a_desc + 4), "l"(b_desc + 4), "l"(a_desc + 6), "l"(b_desc + 6)
+      : "memory");
+  return r;
+}
+
 // arrive on `bar` once every tcgen05 operation issued so far by this thread has completed
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
