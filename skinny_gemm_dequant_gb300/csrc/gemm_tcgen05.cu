@@ -201,19 +201,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t par = 0;
     uint64_t aoff = 0, boff = 0;
     uint32_t sfoff = 0;
+    uint32_t ready = 0;  // bits 0 / 1: this stage's TMA / scale barriers already seen complete
     for (int kt = 0; kt < nk; ++kt) {
-      if (!mbar_wait(&tma_full[s], par, lim, abort) || !mbar_wait(&sf_full[s], par, lim, abort)) {
+      if ((!(ready & 1) && !mbar_wait(&tma_full[s], par, lim, abort)) ||
+          (!(ready & 2) && !mbar_wait(&sf_full[s], par, lim, abort))) {
         fail();
         break;
       }
       tc_fence_after();
       const uint64_t ad = a_desc0 + aoff, bd = b_desc0 + boff;
       const uint32_t sfa = tmem + kSfCol0 + sfoff;
-      // four 32-K steps (32 bytes = 2 descriptor units each), scale byte j of each vector
+      // four 32-K steps (32 bytes = 2 descriptor units each), scale byte j of each vector; the
+      // next stage's barriers are tested while the first token tile's MMAs issue
+      const int sn = s + 1 == S ? 0 : s + 1;
+      const uint32_t pn = s + 1 == S ? par ^ 1u : par;
+      ready = mma4_mxf8f6f4_test2(tmem, ad, bd, idesc, sfa, sfa + 4, kt > 0 ? 1u : 0u, smem_u32(&tma_full[sn]),
+                                  smem_u32(&sf_full[sn]), pn);
+      if (two) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        mma_mxf8f6f4(tmem, ad + 2 * j, bd + 2 * j, idesc[j], sfa, sfa + 4, (kt > 0 || j > 0) ? 1u : 0u);
-        if (two)
+        for (int j = 0; j < 4; ++j)
           mma_mxf8f6f4(tmem + (uint32_t)p.sub_n, ad + 2 * j, bd + b_sub + 2 * j, idesc[j], sfa, sfa + 8,
                        (kt > 0 || j > 0) ? 1u : 0u);
       }

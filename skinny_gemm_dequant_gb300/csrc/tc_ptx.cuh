@@ -147,6 +147,34 @@ __device__ __forceinline__ uint32_t mma4_f16_test2(uint32_t d_tmem, uint64_t a_d
   return r;
 }
 
+// One stage of block-scaled MMAs (four K = 32 steps, scale byte j of each vector chosen by
+// idesc j) issued in the same instruction stream as a non-blocking test of the next stage's two
+// barriers, as mma4_f16_test2.  Returns bit 0 / bit 1 = barrier 0 / 1 complete.
+__device__ __forceinline__ uint32_t mma4_mxf8f6f4_test2(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                        const uint32_t (&idesc)[4], uint32_t sfa_tmem,
+                                                        uint32_t sfb_tmem, uint32_t accumulate, uint32_t bar0,
+                                                        uint32_t bar1, uint32_t parity) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p0, p1, pa;\n\t.reg .u32 r0, r1;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p0, [%5], %7;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p1, [%6], %7;\n\t"
+      "setp.ne.b32 pa, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %2, %3, %8, [%12], [%13], pa;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %14, %15, %9, [%12], [%13], 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %16, %17, %10, [%12], [%13], 1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%1], %18, %19, %11, [%12], [%13], 1;\n\t"
+      "selp.u32 r0, 1, 0, p0;\n\t"
+      "selp.u32 r1, 2, 0, p1;\n\t"
+      "or.b32 %0, r0, r1;\n\t}"
+      : "=r"(r)
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(accumulate), "r"(bar0), "r"(bar1), "r"(parity), "r"(idesc[0]),
+        "r"(idesc[1]), "r"(idesc[2]), "r"(idesc[3]), "r"(sfa_tmem), "r"(sfb_tmem), "l"(a_desc + 2), "l"(b_desc + 2),
+        "l"(a_desc + 4), "l"(b_desc + 4), "l"(a_desc + 6), "l"(b_desc + 6)
+      : "memory");
+  return r;
+}
+
 // arrive on `bar` once every tcgen05 operation issued so far by this thread has completed
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
