@@ -199,6 +199,23 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workloads (GPU)
+def static_cfg(name):
+    """The `config` object of a workload: the same for both arms (it describes the work, not
+    the device)."""
+    if name in ("c0", "c1", "n1"):
+        shapes = [(512, 1024)] if name == "c0" else C1_SHAPES
+        Ms = {"c0": [1], "c1": C1_MS, "n1": N1_MS}[name]
+        return {"workload": WORKLOADS[name], "shapes": [list(x) for x in shapes], "M": Ms}
+    if name in ("c3", "n3", "n5"):
+        return {"workload": WORKLOADS[name], "bytes": "unique touched experts x 13369344 B + x + logits + y"}
+    return {"workload": WORKLOADS[name]}
+
+
+def arm_config(name, ws):
+    return dict(static_cfg(name), parallelism=f"replicas x{ws}",
+                l2="weights rotate over 6 copies per shape (inputs larger than L2)")
+
+
 class Workload:
     """A list of calls; each call(i) enqueues one layer call on the current stream."""
 
@@ -235,14 +252,11 @@ def build_c1(ql, torch, shapes=C1_SHAPES, Ms=C1_MS, name="c1"):
 
             calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": bytes_int8(M, N, K), "flops": 2 * M * N * K,
                           "x": x, "y": y, "kind": "int8"})
-    cfg = {"workload": WORKLOADS[name], "shapes": [list(s) for s in shapes], "M": Ms}
-    return Workload(name, calls, len(calls), cfg)  # one fused launch per call
+    return Workload(name, calls, len(calls), static_cfg(name))  # one fused launch per call
 
 
 def build_c0(ql, torch):
-    w = build_c1(ql, torch, shapes=[(512, 1024)], Ms=[1], name="c0")
-    w.cfg = {"workload": WORKLOADS["c0"], "shapes": [[512, 1024]], "M": [1]}
-    return w
+    return build_c1(ql, torch, shapes=[(512, 1024)], Ms=[1], name="c0")
 
 
 def build_c2(ql, torch):
@@ -266,8 +280,7 @@ def build_c2(ql, torch):
 
             calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": bytes_fp8(M, N, K), "flops": 2 * M * N * K,
                           "x": x, "y": y, "kind": "fp8"})
-    cfg = {"workload": WORKLOADS["c2"]}
-    return Workload("c2", calls, len(calls), cfg)
+    return Workload("c2", calls, len(calls), static_cfg("c2"))
 
 
 def build_c3(ql, torch, limit=None, name="c3", Ms=None):
@@ -297,8 +310,7 @@ def build_c3(ql, torch, limit=None, name="c3", Ms=None):
                       "x": sets[0][0], "y": y, "kind": "moe_tcgen05" if grouped else "moe",
                       "inputs": [t for st in sets for t in st[:2]],  # every rotation's x and logits
                       "unique_experts": uniq})
-    cfg = {"workload": WORKLOADS[name],
-           "bytes": "unique touched experts x 13369344 B + x + logits + y"}
+    cfg = static_cfg(name)
     # skinny path: gate_up (with routing), down, combine; grouped path: routing, dispatch,
     # quantise-and-scatter, gate_up GEMM, h quantisation, down GEMM, combine
     return Workload(name, calls, (7 if grouped else 3) * len(calls), cfg)
@@ -351,8 +363,7 @@ def build_c4(ql, torch):
                 b = bytes_mxfp4(M, N, K)
             calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": b, "flops": 2 * M * N * K, "x": x, "y": y,
                           "kind": kind + "_tcgen05"})
-    cfg = {"workload": WORKLOADS["c4"]}
-    return Workload("c4", calls, 2 * len(calls), cfg)
+    return Workload("c4", calls, 2 * len(calls), static_cfg("c4"))
 
 
 N4_MS = [1, 4, 16]
@@ -379,8 +390,7 @@ def build_n4(ql, torch):
 
             calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": bytes_bf16(M, N, K), "flops": 2 * M * N * K,
                           "x": x, "y": y, "kind": "bf16"})
-    cfg = {"workload": WORKLOADS["n4"]}
-    return Workload("n4", calls, len(calls), cfg)
+    return Workload("n4", calls, len(calls), static_cfg("n4"))
 
 
 N1_MS = [32, 64, 128, 256]
@@ -424,8 +434,7 @@ def build_n2(ql, torch):
 
             calls.append({"fn": call, "M": M, "N": N, "K": K, "bytes": bytes_fp8c(M, N, K), "flops": 2 * M * N * K,
                           "x": x, "y": y, "kind": "fp8_channel"})
-    cfg = {"workload": WORKLOADS["n2"]}
-    return Workload("n2", calls, len(calls), cfg)
+    return Workload("n2", calls, len(calls), static_cfg("n2"))
 
 
 BUILDERS = {"c0": build_c0, "c1": build_c1, "c2": build_c2, "c3": build_c3, "c4": build_c4, "n1": build_n1, "n2": build_n2,
@@ -708,10 +717,17 @@ def job_throughput(bytes_per_rank_step, steps, ms_max, world):
 def run_reference(args, ws, rank):
     if rank != 0:
         return
-    # the oracle as it stands, its sampled rows split over one thread per host core
+    # the oracle as it stands, its sampled rows split over one thread per host core; the sample
+    # grows (64 rows a call, x4, up to 4096) until a step takes its share of about 90 s for the
+    # whole run, so the per-call work that does not scale with the rows (the activation
+    # quantisation of every call) does not dominate a short step
     cores = host_cores()
+    per_step = min(5.0, max(0.25, 90.0 / max(1, args.steps + args.warmup)))
     rows = 64
     jobs, bb, desc = oracle_jobs(args.config, rows, cores)
+    while rows < 4096 and time_jobs(jobs, cores) < per_step / 4:
+        rows *= 4
+        jobs, bb, desc = oracle_jobs(args.config, rows, cores)
     for _ in range(args.warmup):
         time_jobs(jobs, cores)
     t = 0.0
@@ -723,7 +739,7 @@ def run_reference(args, ws, rank):
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPES[args.config],
-            "data": "synthetic", "config": {"workload": WORKLOADS[args.config]},
+            "data": "synthetic", "config": arm_config(args.config, ws),
             "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cores, "threads": cores, "kind": "oracle",
                              "sample": desc + f" ({rows} rows per call per step, split over {cores} threads)"},
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -819,8 +835,7 @@ def main():
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": DTYPES[args.config], "data": "synthetic",
-            "config": dict(wl.cfg, parallelism=f"replicas x{ws}", l2="weights rotate over 6 copies per shape "
-                                                                   "(inputs larger than L2)"),
+            "config": arm_config(args.config, ws),
             "us_per_call_mean": round(ms_step * 1e3 / len(wl.calls), 3),
             "calls": calls, "roofline": roofline,
             "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
