@@ -247,7 +247,8 @@ QL_API ql_status qlinear_bf16(const uint16_t* x, int64_t M, int64_t K, int64_t l
  * h_out bf16 [M*topk, I] (row m*topk + j).
  * swiglu_alpha must be finite; swiglu_limit >= 0 (+infinity allowed), else QL_ERR_INVALID_ARG.
  * Paths: M <= 16: the persistent skinny kernel with bf16 activations (routing fused into the
- *        gate_up launch), QL_PATH_MOE_MXFP4;
+ *        gate_up launch), QL_PATH_MOE_MXFP4; 9..16 tokens run as two such calls, tokens
+ *        [0, 8) and [8, M) (tokens are independent; one 8-token tile per call is cheaper);
  *        M > 16: grouped tcgen05 GEMMs over the routed experts ([DSV4] §0.3 grouped batch MoE),
  *        QL_PATH_MOE_MXFP4_TCGEN05: x and h are quantised per token and 128-K group to E4M3 with
  *        a UE8M0 scale before their GEMMs (the activation format of qlinear_mxfp4's act_mode 1).
