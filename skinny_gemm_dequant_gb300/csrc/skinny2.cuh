@@ -442,6 +442,93 @@ __device__ void s2_local_image(const Skinny2Args& a, uint32_t L, int kt0, int n_
   }
 }
 
+// The same image for 2..8 tokens in one pass over the rows: thread tid reads token tid % M
+// (eight of its vectors in flight at a time) for the token's amax, and stores the vectors of
+// this CTA's own units raw into their image slots on the way; the per-token maxima meet in
+// shared memory, and the slots are then converted in place (a bf16 vector and its f16 image
+// are both 16 bytes).  Token by token (s2_local_image) took an L2 round trip and two barriers
+// per token.  red: >= 24 floats, red[0, 8) zero on entry (per-token amax bits, then factors).
+template <int FMT>
+__device__ void s2_local_image_multi(const Skinny2Args& a, uint32_t L, int kt0, int n_slots, int tid, float* red,
+                                     float* tokf) {
+  constexpr int KPU = S2Traits<FMT>::KPU, VPU = KPU / 8;
+  const int nvec = a.K / 8, M = a.M, nk = a.nk;
+  const uint32_t slot_bytes = (uint32_t)(S2Traits<FMT>::NXB * M * 128);
+  auto slot_addr = [&](int sl, int c8, int m) {
+    const int jj = c8 >> 3, c16 = c8 & 7;  // slab, 16-byte chunk of the 128-byte row
+    return L + (uint32_t)sl * slot_bytes + (uint32_t)(jj * M + m) * 128u + (uint32_t)((c16 ^ (m & 7)) << 4);
+  };
+  const int m = tid % M, ti = tid / M, nth = (255 - m) / M + 1;  // this thread's token, rank, peers
+  const uint16_t* xr = a.x + (int64_t)m * a.ldx;
+  float am = 0.f;
+#pragma unroll 1
+  for (int i0 = ti; i0 < nvec; i0 += 8 * nth) {
+    uint4 u[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int i = i0 + r * nth;
+      if (i < nvec) u[r] = *reinterpret_cast<const uint4*>(xr + 8 * i);
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const int i = i0 + r * nth;
+      if (i >= nvec) break;
+      am = fmaxf(am, fmaxf(fmaxf(bf16x2_absmax(u[r].x), bf16x2_absmax(u[r].y)),
+                           fmaxf(bf16x2_absmax(u[r].z), bf16x2_absmax(u[r].w))));
+      const int kt = i / VPU, c8 = i - kt * VPU;
+      int sl = kt - kt0;
+      if (sl < 0) sl += nk;
+      if (sl < n_slots)
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(slot_addr(sl, c8, m)), "r"(u[r].x), "r"(u[r].y),
+                     "r"(u[r].z), "r"(u[r].w)
+                     : "memory");
+    }
+  }
+  // own vectors past the row's end (K not a multiple of the unit): zeros
+  for (int t = tid; t < n_slots * VPU; t += 256) {
+    const int sl = t / VPU, c8 = t - sl * VPU;
+    int kt = kt0 + sl;
+    if (kt >= nk) kt -= nk;
+    if (kt * VPU + c8 < nvec) continue;
+    for (int mm = 0; mm < M; ++mm)
+      asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(slot_addr(sl, c8, mm)), "r"(0u) : "memory");
+  }
+  // non-negative floats order as their bit patterns
+  atomicMax(reinterpret_cast<int*>(red) + m, __float_as_int(am));
+  consumer_sync();
+  if (tid < M) {
+    float amax = red[tid];
+    if (FMT == FMT_INT8 && a.amax_in) amax = a.amax_in[tid];  // a K shard: the whole row's amax
+    float f, inv;
+    bool fast;
+    s2_token_factors<FMT>(amax, f, inv, fast);
+    tokf[tid] = f;
+    red[8 + tid] = inv;
+    red[16 + tid] = fast ? 1.f : 0.f;
+    if (FMT == FMT_INT8 && a.xs_dbg && blockIdx.x == 0) a.xs_dbg[tid] = f;
+  }
+  consumer_sync();
+  // in place: one copy of the conversion code (it runs once per call, from a cold instruction cache)
+#pragma unroll 1
+  for (int e = tid; e < n_slots * VPU * M; e += 256) {
+    const int mm = e % M, t = e / M;
+    const int sl = t / VPU, c8 = t - sl * VPU;
+    const uint32_t ad = slot_addr(sl, c8, mm);
+    uint4 u;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w) : "r"(ad));
+    uint32_t h[4], qb[2];
+    s2_conv8<FMT>(u, tokf[mm], red[8 + mm], red[16 + mm] != 0.f, h, qb);
+    int kt = kt0 + sl;
+    if (kt >= nk) kt -= nk;
+    const int k = kt * KPU + c8 * 8;
+    if (FMT == FMT_INT8 && a.xq_dbg && k < a.K)
+      *reinterpret_cast<uint2*>(a.xq_dbg + (int64_t)mm * a.K + k) = make_uint2(qb[0], qb[1]);
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(ad), "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                 : "memory");
+  }
+  consumer_sync();
+}
+
 // MoE down activations, one job = (dispatch position q, slice sl of nsl).  The pair p = m*topk+j
 // at position q went to expert e; its gate and up sums g, u (length I) are gu[p].  Its activation
 // row is h = bf16(silu(g) * u), or with a clamp bf16(silu(alpha min(g, limit)) clamp(u, +-limit))

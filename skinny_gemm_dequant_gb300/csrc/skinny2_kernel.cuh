@@ -15,6 +15,10 @@
 #pragma once
 #include "skinny2.cuh"
 
+#ifndef QL_LOCAL_MULTI
+#define QL_LOCAL_MULTI 1
+#endif
+
 namespace ql {
 
 // tmW: 4D view {128 bytes, N rows, full 128-byte chunks, experts} (strides ldw, 128, expert
@@ -79,7 +83,7 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
   // job and count them in with one release (the rows are read by TMA, the async proxy, in other
   // CTAs: proxy fence first; the release is cumulative over the CTA's writes, ordered before it
   // by the barrier)
-  __shared__ float s_red[S2_CONSUMERS];
+  __shared__ float s_red[3 * S2_CONSUMERS];  // a job's 8 warp maxima; local multi-token images: 3 per token
   auto run_jobs = [&](int njob_rows, int nsl) {
     unsigned mine = 0;
     for (int j = c; j < njob_rows * nsl; j += G, ++mine) {
@@ -142,6 +146,8 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
     }
     tc::fence_mbar_init();
     s_abort = 0;
+    if constexpr (kLocal)
+      for (int i = 0; i < 8; ++i) s_red[i] = 0.f;  // multi-token local images: per-token amax maxima
     tc::tma_prefetch_desc(&tmW);
     tc::tma_prefetch_desc(&tmX);
   }
@@ -369,8 +375,18 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
   // CTA's jobs of the activation image (gate_up wrote them before routing)
   pdl_wait();
   const int kt0c = (int)(s0 - (int64_t)rb_first * nk);  // K unit of this CTA's first unit
-  if constexpr (kLocal)
-    s2_local_image<FMT>(a, tc::smem_u32(limg), kt0c, (int)min(s1 - s0, (int64_t)nk), threadIdx.x, s_red, s_tokf);
+  if constexpr (kLocal) {
+#if QL_LOCAL_MULTI
+    // one pass over all rows when it takes fewer rounds of eight loads per thread than the
+    // token-by-token build takes tokens (measured: 4 tokens x K = 5120 -0.8 us a call, 2 tokens x
+    // K = 17408 +0.8 us)
+    if (a.M > 1 && (a.K / 8 * a.M + 2047) / 2048 < a.M)
+      s2_local_image_multi<FMT>(a, tc::smem_u32(limg), kt0c, (int)min(s1 - s0, (int64_t)nk), threadIdx.x, s_red,
+                                s_tokf);
+    else
+#endif
+      s2_local_image<FMT>(a, tc::smem_u32(limg), kt0c, (int)min(s1 - s0, (int64_t)nk), threadIdx.x, s_red, s_tokf);
+  }
   else if constexpr (KIND != S2_MOE_GU)
     run_jobs(njob_rows, nsl);
   const int g = lane >> 2, t = lane & 3;

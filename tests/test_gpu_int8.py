@@ -48,6 +48,14 @@ def test_int8_small(ql, M, N, K):
     compare(c, run(ql, c))
 
 
+@pytest.mark.parametrize("M,N,K", [(2, 3000, 1008), (7, 3000, 1008), (8, 5000, 5120), (4, 9000, 2000)])
+def test_int8_local_image_multi_token(ql, M, N, K):
+    # M * K <= 40960: every CTA builds its own image of 2..8 tokens in one pass over the rows,
+    # K ragged against the 256-K unit (zero tails in the last unit's slots)
+    c = synth.int8_case(M, N, K, seed=M * 7 + K)
+    compare(c, run(ql, c))
+
+
 def test_int8_many_tokens_chunked(ql):
     c = synth.int8_case(37, 96, 512, seed=3)
     compare(c, run(ql, c))
