@@ -101,6 +101,20 @@ def test_moe_persistent_given_ids(ql):
     check_moe(c, got, I, topk, ids=ids, wts=wts)
 
 
+def test_moe_persistent_given_ids_more_than_8_tokens(ql):
+    # 9..16 tokens run as two calls of 8 and M - 8 tokens: the given ids and weights, the debug
+    # outputs and y of the second call sit at row 8 of every array
+    E, H, I, topk, M = 8, 256, 512, 3, 13
+    c = synth.moe_case(M, E, H, I, seed=34)
+    wdev = [torch.from_numpy(c[k]).cuda() for k in ("w13", "s13", "w2", "s2")]
+    r = synth.rng(34, 7)
+    ids = np.stack([r.permutation(E)[:topk] for _ in range(M)]).astype(np.int32)
+    wts = r.uniform(0.05, 1.0, (M, topk)).astype(np.float32)
+    got = run_moe(ql, c, wdev, topk, ids=ids, wts=wts)
+    assert np.array_equal(got[1], ids)
+    check_moe(c, got, I, topk, ids=ids, wts=wts)
+
+
 def test_moe_given_ids_and_renormalised_routing(ql):
     E, H, I, topk = 8, 128, 128, 2
     c = synth.moe_case(4, E, H, I, seed=31)
