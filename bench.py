@@ -311,9 +311,11 @@ def build_c3(ql, torch, limit=None, name="c3", Ms=None):
                       "inputs": [t for st in sets for t in st[:2]],  # every rotation's x and logits
                       "unique_experts": uniq})
     cfg = static_cfg(name)
-    # skinny path: gate_up (with routing), down, combine; grouped path: routing, dispatch,
-    # quantise-and-scatter, gate_up GEMM, h quantisation, down GEMM, combine
-    return Workload(name, calls, (7 if grouped else 3) * len(calls), cfg)
+    # skinny path: gate_up (with routing), down, combine, twice for 9..16 tokens (two calls of 8
+    # and M - 8 tokens); grouped path: routing, dispatch, quantise-and-scatter, gate_up GEMM,
+    # h quantisation, down GEMM, combine
+    launches = sum(7 if grouped else (6 if c["M"] > 8 else 3) for c in calls)
+    return Workload(name, calls, launches, cfg)
 
 
 N5_MS = [32, 64, 128, 256]
