@@ -35,6 +35,8 @@ constexpr int kBlockN = 128;  // weight rows per CTA (MMA M)
 constexpr int kBlockK = 128;  // K elements per stage
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;  // scale vectors live after the (<= 256-column) accumulator
+constexpr uint32_t kSfColResident = 128;  // resident scale vectors: after a <= 128-column accumulator
+constexpr int kResidentFirst = 8;  // resident scales: stages written before the MMAs may start
 constexpr uint32_t kDrainLimit = 1u << 22;
 
 struct TcParams {
@@ -52,6 +54,11 @@ struct TcParams {
   uint32_t wait_limit;
   int sf_layout;  // 0: row r at (lane r % 32 of every quadrant, column r / 32); 1: (lane r, column 0)
   int staged;     // 1: every scale byte of the CTA is copied to shared memory once, at the start
+  // 1 (staged, one token sub-tile of <= 128 columns, every stage's scale vectors fit in tensor
+  // memory behind the accumulator): the scale writers put all of them in tensor memory before
+  // the MMAs need them, instead of one ring slot per stage (which paced the MMAs: the writer
+  // sharing a scheduler with the MMA-issuing warp fell ~0.45 us behind every stage)
+  int resident;
   uint32_t sc_w_bytes;  // shared-memory bytes of the staged weight scales (16-byte multiple)
   // grouped (MoE) launches: blockIdx.y indexes a tile list built on the device
   int grouped;
@@ -202,7 +209,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t aoff = 0, boff = 0;
     uint32_t sfoff = 0;
     uint32_t ready = 0;  // bits 0 / 1: this stage's TMA / scale barriers already seen complete
+    const uint32_t sf_base = p.resident ? kSfColResident : kSfCol0;
     for (int kt = 0; kt < nk; ++kt) {
+      if (p.resident) {
+        // resident scales: the first stages' vectors before stage 0, the rest before stage 8
+        if ((kt == 0 || kt == kResidentFirst) && !mbar_wait(&sf_full[kt == 0 ? 0 : 1], 0, lim, abort)) {
+          fail();
+          break;
+        }
+        ready |= 2u;
+      }
       if ((!(ready & 1) && !mbar_wait(&tma_full[s], par, lim, abort)) ||
           (!(ready & 2) && !mbar_wait(&sf_full[s], par, lim, abort))) {
         fail();
@@ -210,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint64_t ad = a_desc0 + aoff, bd = b_desc0 + boff;
-      const uint32_t sfa = tmem + kSfCol0 + sfoff;
+      const uint32_t sfa = tmem + sf_base + sfoff;
       // four 32-K steps (32 bytes = 2 descriptor units each), scale byte j of each vector; the
       // next stage's barriers are tested while the first token tile's MMAs issue
       const int sn = s + 1 == S ? 0 : s + 1;
@@ -231,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s = 0;
         par ^= 1u;
         aoff = boff = 0;
-        sfoff = 0;
+        if (!p.resident) sfoff = 0;  // resident scales: one column group per stage, no ring
       }
     }
     tc_commit(acc_full);  // completes once every MMA issued above has finished
@@ -312,9 +328,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 #pragma unroll
     for (int d = 0; d < kPD; ++d) fetch(d, pw[d], pb[d]);
+    if (p.resident) {
+      // every stage's vectors at its own columns, no ring and no wait: the MMAs start once the
+      // first kResidentFirst stages are in (sf_full[0]) and take the rest after sf_full[1]
+      const int first = nk < kResidentFirst ? nk : kResidentFirst;
+      for (int kt = 0; kt < nk; ++kt) {
+        uint32_t wa[4], wb[2][4];
+        fetch(kt, wa, wb);
+        const uint32_t sf_col = kSfColResident + (uint32_t)kt * (4 + 4 * p.nsub);
+        tmem_st_x4(tmem + lane_base + sf_col, wa[0], wa[1], wa[2], wa[3]);
+        tmem_st_x4(tmem + lane_base + sf_col + 4, wb[0][0], wb[0][1], wb[0][2], wb[0][3]);
+        if (kt + 1 == first || kt + 1 == nk) {
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sf_full[kt + 1 == first ? 0 : 1]);
+        }
+      }
+    }
     int s = 0;
     uint32_t ph = 1;  // parity of the slot's previous use (a fresh barrier passes parity 1)
-    for (int k0 = 0; k0 < nk && ok; k0 += kPD) {
+    for (int k0 = 0; k0 < nk && ok && !p.resident; k0 += kPD) {
 #pragma unroll
       for (int d = 0; d < kPD; ++d) {
         const int kt = k0 + d;
@@ -463,6 +497,13 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   int S = (int)((budget - extra) / stage);
   if (S > 8) S = 8;
   p.stages = S;
+#ifndef QL_RESIDENT_SCALES
+#define QL_RESIDENT_SCALES 1
+#endif
+  p.resident = (QL_RESIDENT_SCALES && p.staged && p.nsub == 1 && p.tt <= (int)kSfColResident &&
+                kSfColResident + (uint32_t)nk * (4 + 4 * (uint32_t)p.nsub) <= kTmemCols)
+                   ? 1
+                   : 0;
   p.ws = g.ws;
   p.lds = g.lds;
   p.as = g.as;
