@@ -37,6 +37,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;  // scale vectors live after the (<= 256-column) accumulator
 constexpr uint32_t kSfColResident = 128;  // resident scale vectors: after a <= 128-column accumulator
 constexpr int kResidentFirst = 8;  // resident scales: stages written before the MMAs may start
+#ifndef QL_RESIDENT_SCALES
+#define QL_RESIDENT_SCALES 1  // 0: every call writes its scale vectors into the ring, stage by stage
+#endif
 constexpr uint32_t kDrainLimit = 1u << 22;
 
 struct TcParams {
@@ -497,9 +500,6 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   int S = (int)((budget - extra) / stage);
   if (S > 8) S = 8;
   p.stages = S;
-#ifndef QL_RESIDENT_SCALES
-#define QL_RESIDENT_SCALES 1
-#endif
   p.resident = (QL_RESIDENT_SCALES && p.staged && p.nsub == 1 && p.tt <= (int)kSfColResident &&
                 kSfColResident + (uint32_t)nk * (4 + 4 * (uint32_t)p.nsub) <= kTmemCols)
                    ? 1
