@@ -61,6 +61,7 @@ struct I8Params {
   int32_t* acc_out;
   uint32_t* status;
   uint32_t wait_limit;
+  int tma_y;  // 1: the output tile leaves through shared memory and one TMA store (tmY)
 };
 
 // ------------------------------------------------------------------ activation quantisation
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(256) quant_i8_image_kernel(const uint16_t* __r
 template <bool kSplit>
 __global__ void __launch_bounds__(kI8Threads, 1)
     i8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ I8Params p) {
+                   const __grid_constant__ CUtensorMap tmY, const __grid_constant__ I8Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_last;
+  __shared__ float s_xs[128];  // the token tile's x_s, for the epilogue
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * 128;
@@ -394,23 +396,47 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       }
       ok = ok && last;
     }
+    // the tile's x_s into shared memory once, by every drain warp (also after a timeout: all of
+    // them reach the barrier): read from global memory inside the output loop, each value waited
+    // behind the previous outputs' stores, the loop took ~6 us
+    pdl_wait();  // x_s comes from the quantisation kernel
+    {
+      const int i = threadIdx.x - 256;  // drain threads are 256..511
+      if (i < p.tt) s_xs[i] = t0 + i < p.M ? p.x_s[t0 + i] : 0.f;
+    }
+    asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight drain warps
+    // with a TMA store, the tile [tt tokens][128 rows] of bf16 goes to shared memory first: the
+    // stage ring is idle once the last group has drained (its loads were all consumed)
+    uint16_t* tile = reinterpret_cast<uint16_t*>(smem);
     if (ok) {
-      pdl_wait();  // x_s comes from the quantisation kernel
-      if (n < p.N) {
-        const float ws = p.w_s ? p.w_s[p.w_s_len > 1 ? n : 0] : 0.f;
-        const float bias = p.bias ? bf16_bits_to_f32(p.bias[n]) : 0.f;
+      if (n < p.N || p.tma_y) {
+        const float ws = (p.w_s && n < p.N) ? p.w_s[p.w_s_len > 1 ? n : 0] : 0.f;
+        const float bias = (p.bias && n < p.N) ? bf16_bits_to_f32(p.bias[n]) : 0.f;
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const int t = t0 + hcol * half + c;
+          const int tl = hcol * half + c, t = t0 + tl;
           if (c < half && t < p.M) {
             const int32_t a = sum[c];
-            if (p.acc_out) p.acc_out[(int64_t)t * p.N + n] = a;
+            if (p.acc_out && n < p.N) p.acc_out[(int64_t)t * p.N + n] = a;
             if (!p.y) continue;  // a K shard: the int32 sums are the result
-            uint16_t yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)a, p.x_s[t]), ws));
+            uint16_t yb = f32_to_bf16_rn(__fmul_rn(__fmul_rn((float)a, s_xs[tl]), ws));
             if (p.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + bias);
-            p.y[(int64_t)t * p.ldy + n] = yb;
+            if (p.tma_y)
+              tile[tl * 128 + 32 * q + lane] = yb;
+            else
+              p.y[(int64_t)t * p.ldy + n] = yb;
           }
         }
+      }
+    }
+    if (p.tma_y) {
+      // every drain warp reaches the barrier; the store goes out only from a CTA holding the
+      // finished sums (with split K: the one that added the splits) and without a timeout
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> TMA reads
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (threadIdx.x == 256 && (!kSplit || s_last) && !*abort) {
+        tma_store_2d(&tmY, smem_u32(tile), n0, t0);
+        bulk_commit_and_wait_all();
       }
     }
   }
@@ -492,7 +518,7 @@ cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st) {
   p.part = g.part;
   p.tickets = g.tickets;
   const size_t stage = (size_t)kI8A8Bytes + kI8A16Bytes + (size_t)p.tt * kI8BlockK * 2;
-  const size_t budget = 227 * 1024 - 1024 - 256;
+  const size_t budget = 227 * 1024 - 1024 - 1024;  // alignment slack, static shared memory
   int S = (int)(budget / stage);
   if (S > 8) S = 8;
   p.stages = S;
@@ -514,6 +540,16 @@ cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st) {
       !i8_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, g.img, (uint64_t)kpad, (uint64_t)g.M, (uint64_t)kpad * 2, kI8BlockK,
               (uint32_t)p.tt, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  // the output: bf16 [M][ldy], stored a [tt][128] box per CTA when its rows can be TMA rows
+  // (16-byte aligned base and row pitch) and K is not split (measured: M = 128 / 256 at
+  // 17408x5120 -1.6 / -3.3 us a call; the split calls at 5120x17408 +1.1 us); else the drain
+  // warps store it element by element
+  CUtensorMap ty = ta;
+  p.tma_y = 0;
+  if (g.y && p.ks == 1 && (reinterpret_cast<uintptr_t>(g.y) & 15) == 0 && (g.ldy * 2) % 16 == 0 &&
+      i8_map(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.y, (uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.ldy * 2, 128,
+             (uint32_t)p.tt, CU_TENSOR_MAP_SWIZZLE_NONE))
+    p.tma_y = 1;
 
   const size_t smem = 1024 + (size_t)S * stage + (size_t)(3 * S + 5) * 8;
   static std::atomic<int> attr{0};
@@ -533,8 +569,8 @@ cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return p.ks > 1 ? cudaLaunchKernelEx(&cfg, i8_gemm_kernel<true>, ta, tb, p)
-                  : cudaLaunchKernelEx(&cfg, i8_gemm_kernel<false>, ta, tb, p);
+  return p.ks > 1 ? cudaLaunchKernelEx(&cfg, i8_gemm_kernel<true>, ta, tb, ty, p)
+                  : cudaLaunchKernelEx(&cfg, i8_gemm_kernel<false>, ta, tb, ty, p);
 }
 
 }  // namespace tc
