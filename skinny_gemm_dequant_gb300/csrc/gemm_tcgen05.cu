@@ -62,6 +62,7 @@ struct TcParams {
   // the MMAs need them, instead of one ring slot per stage (which paced the MMAs: the writer
   // sharing a scheduler with the MMA-issuing warp fell ~0.45 us behind every stage)
   int resident;
+  int tma_y;  // 1: the output tile leaves through shared memory and one TMA store (tmY)
   uint32_t sc_w_bytes;  // shared-memory bytes of the staged weight scales (16-byte multiple)
   // grouped (MoE) launches: blockIdx.y indexes a tile list built on the device
   int grouped;
@@ -87,7 +88,7 @@ __device__ __forceinline__ uint32_t rep4(uint32_t b) { return (b & 0xFFu) * 0x01
 
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ TcParams p) {
+                   const __grid_constant__ CUtensorMap tmY, const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
@@ -405,7 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               } else {
                 uint16_t yb = f32_to_bf16_rn(__uint_as_float(r[j]));
                 if (p.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + bias);
-                p.y[(int64_t)(t0 + tc) * p.ldy + n] = yb;
+                if (p.tma_y)  // [tt][128] tile in the idle stage ring, stored below
+                  reinterpret_cast<uint16_t*>(smem)[tc * kBlockN + 32 * q + lane] = yb;
+                else
+                  p.y[(int64_t)(t0 + tc) * p.ldy + n] = yb;
               }
             }
           }
@@ -413,6 +417,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (ok && lane == 0) {
       fail();
+    }
+    if (p.tma_y) {
+      // every epilogue warp reaches the barrier; the tile goes out in one store unless a wait
+      // timed out
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> TMA reads
+      asm volatile("bar.sync 2, 128;" ::: "memory");                // the four epilogue warps
+      if (warp == 4 && lane == 0 && got && !*abort) {
+        tma_store_2d(&tmY, smem_u32(smem), n0, t0);
+        bulk_commit_and_wait_all();
+      }
     }
   }
   tc_fence_before();
@@ -530,6 +544,21 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   const bool ok_b = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.aq, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.K,
                              kBlockK, (uint32_t)p.tt);
   if (!ok_a || !ok_b) return cudaErrorInvalidValue;
+  // the dense output: bf16 [M][ldy], stored a [tt][128] box per CTA when its rows can be TMA rows
+  // (16-byte aligned base and row pitch); else the epilogue warps store it element by element
+  CUtensorMap ty = ta;
+  p.tma_y = 0;
+  if (!g.grouped && g.y && (reinterpret_cast<uintptr_t>(g.y) & 15) == 0 && (g.ldy * 2) % 16 == 0) {
+    auto fn = encode_fn();
+    cuuint64_t dims[2] = {(cuuint64_t)g.N, (cuuint64_t)g.M};
+    cuuint64_t strides[1] = {(cuuint64_t)g.ldy * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBlockN, (cuuint32_t)p.tt};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn && fn(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, g.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      p.tma_y = 1;
+  }
 
   const size_t smem = 1024 + (size_t)S * stage + (size_t)(3 * S + 2) * 8 + extra;
   static std::atomic<int> attr_set{0};
@@ -549,7 +578,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, ta, tb, p);
+  return cudaLaunchKernelEx(&cfg, tc_gemm_kernel, ta, tb, ty, p);
 }
 
 }  // namespace tc
