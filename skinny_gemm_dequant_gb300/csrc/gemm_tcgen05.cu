@@ -385,6 +385,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    // grouped: the tile's pair of every dispatch row into shared memory (every epilogue warp
+    // gets here): read from global memory inside the output loop, each load waited behind the
+    // previous outputs' stores
+    __shared__ int32_t s_pairs[256];
+    if (p.grouped) {
+      for (int i = threadIdx.x - 128; i < p.tt; i += 128) s_pairs[i] = i < ntok ? p.pairs[t0 + i] : 0;
+      asm volatile("bar.sync 2, 128;" ::: "memory");  // the four epilogue warps
+    }
     int got = 0;
     if (ok && lane == 0) got = mbar_wait(acc_full, 0, lim, abort);
     got = __shfl_sync(0xffffffffu, got, 0);
@@ -402,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tc = c0 + j;  // token column
             if (tc < p.tt && tc < ntok) {
               if (p.grouped) {  // fp32 row of the (token, slot) pair at this dispatch row
-                p.out[(int64_t)p.pairs[t0 + tc] * p.ld_out + n] = __uint_as_float(r[j]);
+                p.out[(int64_t)s_pairs[tc] * p.ld_out + n] = __uint_as_float(r[j]);
               } else {
                 uint16_t yb = f32_to_bf16_rn(__uint_as_float(r[j]));
                 if (p.bias) yb = f32_to_bf16_rn(bf16_bits_to_f32(yb) + bias);
@@ -504,7 +512,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
   p.sub_n = (((mpad + p.nsub - 1) / p.nsub) + 15) / 16 * 16;
   p.tt = p.nsub * p.sub_n;
   const size_t stage = (size_t)kBlockN * kBlockK + (size_t)p.tt * kBlockK;
-  const size_t budget = 227 * 1024 - 1024 - 256;
+  const size_t budget = 227 * 1024 - 1024 - 2048;  // alignment slack, static shared memory
   const int nk = g.K / kBlockK;
   // stage the scales in shared memory when they take at most 48 KB and leave two stages
   const size_t sc_bytes = sc_w_bytes(g.fp4, nk) + (((size_t)p.tt * nk + 15) & ~(size_t)15);
