@@ -380,15 +380,24 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       if (last) {
         __threadfence();  // the other slots were fenced before their counts
         if (ok && n < p.N) {
+          // every slot from L2, this CTA's own included (stored and fenced above), 32 loads in
+          // flight at a time (integer sums: any order is exact); the loads of one output at a
+          // time took ~33 us at 5120x17408
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const int t = t0 + hcol * half + c;
-            if (c < half && t < p.M) {
-              // every slot from L2, this CTA's own included (stored and fenced above)
-              const int32_t* col = p.part + (int64_t)t * p.N + n;
-              int32_t a = 0;
-              for (int z = 0; z < p.ks; ++z) a += __ldcg(col + (int64_t)z * p.M * p.N);
-              sum[c] = a;
+          for (int c = 0; c < 64; ++c) sum[c] = 0;
+          const int32_t* base = p.part + (int64_t)(t0 + hcol * half) * p.N + n;
+          for (int z = 0; z < p.ks; ++z) {
+            const int32_t* slot_z = base + (int64_t)z * p.M * p.N;
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {  // 32 loads in flight at a time
+              int32_t v[32];
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const int cc = 32 * hb + c;
+                v[c] = (cc < half && t0 + hcol * half + cc < p.M) ? __ldcg(slot_z + (int64_t)cc * p.N) : 0;
+              }
+#pragma unroll
+              for (int c = 0; c < 32; ++c) sum[32 * hb + c] += v[c];
             }
           }
         }
@@ -542,8 +551,8 @@ cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st) {
     return cudaErrorInvalidValue;
   // the output: bf16 [M][ldy], stored a [tt][128] box per CTA when its rows can be TMA rows
   // (16-byte aligned base and row pitch) and K is not split (measured: M = 128 / 256 at
-  // 17408x5120 -1.6 / -3.3 us a call; the split calls at 5120x17408 +1.1 us); else the drain
-  // warps store it element by element
+  // 17408x5120 -1.6 / -3.3 us a call; the split calls at 5120x17408 gain nothing from it);
+  // else the drain warps store it element by element
   CUtensorMap ty = ta;
   p.tma_y = 0;
   if (g.y && p.ks == 1 && (reinterpret_cast<uintptr_t>(g.y) & 15) == 0 && (g.ldy * 2) % 16 == 0 &&
