@@ -550,12 +550,13 @@ cudaError_t launch_i8_gemm(const I8GemmArgs& g, cudaStream_t st) {
               (uint32_t)p.tt, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   // the output: bf16 [M][ldy], stored a [tt][128] box per CTA when its rows can be TMA rows
-  // (16-byte aligned base and row pitch) and K is not split (measured: M = 128 / 256 at
-  // 17408x5120 -1.6 / -3.3 us a call; the split calls at 5120x17408 gain nothing from it);
-  // else the drain warps store it element by element
+  // (16-byte aligned base and row pitch), N is a multiple of 8 (a TMA store clips the inner
+  // dimension at whole 16-byte chunks) and K is not split (measured: M = 128 / 256 at 17408x5120
+  // -1.6 / -3.3 us a call; the split calls at 5120x17408 gain nothing from it); else the drain
+  // warps store it element by element
   CUtensorMap ty = ta;
   p.tma_y = 0;
-  if (g.y && p.ks == 1 && (reinterpret_cast<uintptr_t>(g.y) & 15) == 0 && (g.ldy * 2) % 16 == 0 &&
+  if (g.y && p.ks == 1 && g.N % 8 == 0 && (reinterpret_cast<uintptr_t>(g.y) & 15) == 0 && (g.ldy * 2) % 16 == 0 &&
       i8_map(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.y, (uint64_t)g.N, (uint64_t)g.M, (uint64_t)g.ldy * 2, 128,
              (uint32_t)p.tt, CU_TENSOR_MAP_SWIZZLE_NONE))
     p.tma_y = 1;

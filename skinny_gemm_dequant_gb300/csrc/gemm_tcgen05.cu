@@ -553,10 +553,12 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st) {
                              kBlockK, (uint32_t)p.tt);
   if (!ok_a || !ok_b) return cudaErrorInvalidValue;
   // the dense output: bf16 [M][ldy], stored a [tt][128] box per CTA when its rows can be TMA rows
-  // (16-byte aligned base and row pitch); else the epilogue warps store it element by element
+  // (16-byte aligned base and row pitch) and N is a multiple of 8: a TMA store clips the inner
+  // dimension at whole 16-byte chunks, so a row ending inside one would get the chunk's columns
+  // past N written too; else the epilogue warps store it element by element
   CUtensorMap ty = ta;
   p.tma_y = 0;
-  if (!g.grouped && g.y && (reinterpret_cast<uintptr_t>(g.y) & 15) == 0 && (g.ldy * 2) % 16 == 0) {
+  if (!g.grouped && g.y && g.N % 8 == 0 && (reinterpret_cast<uintptr_t>(g.y) & 15) == 0 && (g.ldy * 2) % 16 == 0) {
     auto fn = encode_fn();
     cuuint64_t dims[2] = {(cuuint64_t)g.N, (cuuint64_t)g.M};
     cuuint64_t strides[1] = {(cuuint64_t)g.ldy * 2};

@@ -177,3 +177,24 @@ def test_int8_gemm_full_size_sampled(ql, N, K, M):
     c = synth.int8_case(M, N, K, seed=1)
     rows = sample_rows(N, seed=M)
     compare(c, run(ql, c), rows=rows)
+
+
+@pytest.mark.parametrize("M,N,offset", [(64, 9736, 0), (100, 9736, 0), (64, 9736, 1), (64, 9732, 0), (64, 300, 0)])
+def test_int8_gemm_output_pitch_and_alignment(ql, M, N, offset):
+    # as the block-scaled GEMM: with 77 row blocks K is not split, so a padded-pitch aligned view
+    # with N a multiple of 8 takes the TMA-store epilogue (ragged N and M clipped); an unaligned
+    # view, an N ending inside a 16-byte chunk, or a split K (N = 300) the element stores; all
+    # equal the dense output, nothing outside the view is written
+    K = 640
+    c = synth.int8_case(M, N, K, seed=78)
+    x, w, s = to_bf16_tensor(c["x"]), torch.from_numpy(c["w"]).cuda(), torch.from_numpy(c["w_s"]).cuda()
+    ref = ql.qlinear_int8_w8a8(x, w, s)
+    big = torch.full((M + 3, N + 44), -7.0, dtype=torch.bfloat16, device="cuda")  # pitch 688 B
+    out = big[:M, offset:offset + N]
+    ql.qlinear_int8_w8a8(x, w, s, out=out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_of(out.contiguous()), bits_of(ref))
+    rest = big.clone()
+    rest[:M, offset:offset + N] = -7.0
+    bad = (rest != -7.0).nonzero().cpu().numpy()
+    assert len(bad) == 0, f"the store wrote outside the output view: {len(bad)} elements, first {bad[:4].tolist()}"

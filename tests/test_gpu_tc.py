@@ -104,3 +104,24 @@ def test_tc_mxfp4_long_k(ql, M, N, K):
     r = Q.mxfp4_act_quant(c0["x"], c0["w"], s_raw)
     assert np.array_equal(aq, r["q"]) and np.array_equal(as_, r["s"])
     check_float(y, r["y_f64"], r["abs_sum"])
+
+
+@pytest.mark.parametrize("M,N,offset", [(64, 304, 0), (100, 304, 0), (100, 304, 1), (100, 300, 0)])
+def test_tc_fp8_output_pitch_and_alignment(ql, M, N, offset):
+    # y written into a wider buffer: a 16-byte aligned view with a padded row pitch and N a
+    # multiple of 8 takes the TMA-store epilogue (ragged N and M clipped by the store), a view
+    # one element off alignment or an N ending inside a 16-byte chunk the element stores; all
+    # equal the dense output bit for bit and write nothing outside the view
+    K = 640
+    c = synth.fp8_block_case(M, N, K, seed=77)
+    x, w, s = to_bf16_tensor(c["x"]), torch.from_numpy(c["w"]).cuda(), torch.from_numpy(c["s"]).cuda()
+    ref = ql.qlinear_fp8_block(x, w, s, K=K, act_mode=ql.ACT_E4M3_1X128)
+    big = torch.full((M + 3, N + 44), -7.0, dtype=torch.bfloat16, device="cuda")  # pitch 688 B
+    out = big[:M, offset:offset + N]
+    ql.qlinear_fp8_block(x, w, s, K=K, act_mode=ql.ACT_E4M3_1X128, out=out)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_of(out.contiguous()), bits_of(ref))
+    rest = big.clone()
+    rest[:M, offset:offset + N] = -7.0
+    bad = (rest != -7.0).nonzero().cpu().numpy()
+    assert len(bad) == 0, f"the store wrote outside the output view: {len(bad)} elements, first {bad[:4].tolist()}"
