@@ -492,17 +492,28 @@ static int64_t i8_tile_tokens(int64_t M) {
   return mpad < 128 ? mpad : 128;  // token columns per CTA; more tokens take more CTAs
 }
 
-// One CTA per SM at most (shared memory), so a call with fewer output tiles than half the SMs
-// leaves most of the GPU idle: split K into whole 512-K groups until the CTAs fill the SMs once
-// (at most 8 splits, at most one split per group).
+// One CTA per SM at most (shared memory), so a call with few output tiles leaves SMs idle and
+// one with a few more than the SMs runs a second, mostly empty wave: split K into whole 512-K
+// groups (at most 8 splits, at most one per group) where that shortens the modelled launch.
 int i8_splits(int64_t M, int64_t N, int64_t K) {
   const int64_t tiles = (N + 127) / 128 * ((M + i8_tile_tokens(M) - 1) / i8_tile_tokens(M));
-  const int64_t groups = (i8_kpad(K) / kI8BlockK + kI8GroupStages - 1) / kI8GroupStages;
-  if (2 * tiles >= kNumSMs) return 1;
-  int64_t ks = kNumSMs / tiles;
-  if (ks > 8) ks = 8;
-  if (ks > groups) ks = groups;
-  return ks < 1 ? 1 : (int)ks;
+  const int64_t stages = i8_kpad(K) / kI8BlockK;
+  const int64_t groups = (stages + kI8GroupStages - 1) / kI8GroupStages;
+  // the launch's modelled time: waves of CTAs (one per SM), each ~0.45 us per 64-K stage of its
+  // range plus a fixed ~8 us (prologue, drain, epilogue), ~12 us with a split (its slots and the
+  // reduction); fewer splits win unless more are 3 % faster.  For 5120 x 17408 at 256 tokens (80
+  // tiles) it picks 3 splits in 2 waves over 1 split in 1 wave on 80 SMs
+  int best = 1;
+  double best_t = 1e30;
+  for (int ks = 1; ks <= 8 && ks <= groups; ++ks) {
+    const int64_t waves = (tiles * ks + kNumSMs - 1) / kNumSMs;
+    const double t = (double)waves * (0.45 * (double)((stages + ks - 1) / ks) + (ks > 1 ? 12.0 : 8.0));
+    if (t < 0.97 * best_t) {
+      best = ks;
+      best_t = t;
+    }
+  }
+  return best;
 }
 
 size_t i8_part_bytes(int64_t M, int64_t N, int64_t K) {
