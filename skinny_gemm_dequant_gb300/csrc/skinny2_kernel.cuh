@@ -764,12 +764,16 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
           }
         } else {
 #pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {  // 64-K halves of the chunk: the FP8 fold granularity
-            float blk[2][MT][4];            // two chains so consecutive MMAs are independent
+          // the chunk's 128 K in two 64-K halves; with blocks of 128 K or more the whole chunk
+          // shares one scale and folds once, else each half folds with its own
+          const bool whole = a.bk_shift >= 7;
+          float blk[2][MT][4];  // two chains so consecutive MMAs are independent
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
+          for (int e = 0; e < 2; ++e)
 #pragma unroll
-              for (int m = 0; m < MT; ++m) blk[e][m][0] = blk[e][m][1] = blk[e][m][2] = blk[e][m][3] = 0.f;
+            for (int m = 0; m < MT; ++m) blk[e][m][0] = blk[e][m][1] = blk[e][m][2] = blk[e][m][3] = 0.f;
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int pc = 4 * hb + j;
@@ -784,13 +788,18 @@ __global__ void __launch_bounds__(S2_THREADS, s2_ctas_per_sm(FMT, MT))
                 mma_f16_16816(blk[j & 1][m], a0, a1, a2, a3, xv.x, xv.y);
               }
             }
-            const int k0 = (kt * S2_CHUNKS + ck) * 128 + 64 * hb;  // first K of this half
-            // block_k is a power of two; K past the last block (zero weights) has no scale byte
-            const float f = k0 < a.K ? ue8m0_to_f32(sc_row[min(k0, a.K - 1) >> a.bk_shift]) : 0.f;
+            if (hb == 1 || !whole) {
+              const int k0 = (kt * S2_CHUNKS + ck) * 128 + (whole ? 0 : 64 * hb);  // first K folded
+              // block_k is a power of two; K past the last block (zero weights) has no scale byte
+              const float f = k0 < a.K ? ue8m0_to_f32(sc_row[min(k0, a.K - 1) >> a.bk_shift]) : 0.f;
 #pragma unroll
-            for (int m = 0; m < MT; ++m)
+              for (int m = 0; m < MT; ++m)
 #pragma unroll
-              for (int r = 0; r < 4; ++r) acc[m][r] = fmaf(blk[0][m][r] + blk[1][m][r], f, acc[m][r]);
+                for (int r = 0; r < 4; ++r) {
+                  acc[m][r] = fmaf(blk[0][m][r] + blk[1][m][r], f, acc[m][r]);
+                  blk[0][m][r] = blk[1][m][r] = 0.f;
+                }
+            }
           }
         }
       }
