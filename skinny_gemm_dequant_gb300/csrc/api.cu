@@ -15,7 +15,7 @@ using namespace ql;
 #define QL_CELL_TOKENS 4
 #endif
 #ifndef QL_LOCAL_MK
-#define QL_LOCAL_MK 40960
+#define QL_LOCAL_MK 18432
 #endif
 
 namespace {
@@ -48,7 +48,10 @@ constexpr int64_t kSkinnyMaxTokens = 32;
 inline int64_t skinny_tokens(int fmt) { return fmt == FMT_INT8 ? kSkinnyMaxTokens : 16; }
 // dense layers whose M * K is at most this build their activation image inside every CTA
 // (each CTA reads the tokens' whole rows, so the cost grows with M * K) instead of sharing one
-// through global memory, which takes a grid-wide hand-off per call
+// through global memory, which takes a grid-wide hand-off per call.  Measured on the INT8 decode
+// shapes: the local image wins at 1 token (K = 5120 and 17408) and at 2 tokens with K = 5120;
+// the shared one at 2 tokens with K = 17408 (21.7 against 22.3 us) and 4 tokens with K = 5120
+// (16.3 against 17.8 us at N = 10240)
 constexpr int64_t kLocalMK = QL_LOCAL_MK;
 constexpr size_t kTicketOff = 256;
 constexpr size_t kRegionsOff = kTicketOff + kZeroRegion;
