@@ -79,8 +79,10 @@ def test_fp8_full_size_sampled(ql, N, K, M):
 
 
 @pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)])
-def test_fp8_full_size_every_row(ql, N, K):
-    c = synth.fp8_block_case(4, N, K, seed=101)
+@pytest.mark.parametrize("M", [1, 4])
+def test_fp8_full_size_every_row(ql, N, K, M):
+    # 1 token: local activation images where they fit; 4 tokens: the shared image
+    c = synth.fp8_block_case(M, N, K, seed=100 + M)
     compare(c, run(ql, c, K), K)
 
 

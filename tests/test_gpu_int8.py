@@ -99,10 +99,12 @@ def test_int8_skinny_up_to_32_tokens(ql, M, N, K):
 
 
 @pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408), (10240, 5120)])
-@pytest.mark.parametrize("M", [4, 16, 32])
+@pytest.mark.parametrize("M", [1, 2, 4, 16, 32])
 def test_int8_full_size_every_row(ql, N, K, M):
-    # every output row against the oracle: units are claimed at run time, so any row block
-    # may be split between CTAs in a different way on each call
+    # every output row against the oracle, for each way the activations reach the CTAs: local
+    # images (1 token, 2 tokens at K = 5120), the shared image with cells (2 tokens at K = 17408,
+    # 4 tokens), partial slots (16 tokens) and four MMA tiles (32 tokens); a row block's units
+    # may be split between CTAs differently per shape
     c = synth.int8_case(M, N, K, seed=100 + M)
     compare(c, run(ql, c))
 
