@@ -68,3 +68,9 @@ def test_bf16_full_size_sampled(ql, N, K, M):
     c = synth.bf16_dense_case(M, N, K, seed=0)
     rows = sample_rows(N, seed=M)
     compare(c, run(ql, c), K, rows=rows)
+
+
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)])
+def test_bf16_full_size_every_row(ql, N, K):
+    c = synth.bf16_dense_case(4, N, K, seed=201)
+    compare(c, run(ql, c), K)

@@ -83,3 +83,11 @@ def test_fp8_channel_full_size_sampled(ql, fmt, N, K, M):
     c = synth.fp8_channel_case(M, N, K, seed=0, w_fmt=fmt)
     rows = sample_rows(N, seed=M)
     compare(c, run(ql, c, fmt), fmt, K, rows=rows)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("N,K", [(17408, 5120), (5120, 17408)])
+def test_fp8_channel_full_size_every_row(ql, fmt, N, K):
+    # every output row of a 1-token call (local activation images where they fit)
+    c = synth.fp8_channel_case(1, N, K, seed=200, w_fmt=fmt)
+    compare(c, run(ql, c, fmt), fmt, K)
